@@ -1,0 +1,315 @@
+"""Pins of the CPU oracle against facts fixed by the pages and by mathematics.
+
+Each test here is chosen so that a plausible slip in the oracle (a dropped scale,
+a transposed operand, an off-by-one causal diagonal, a wrong GQA head map, a
+wrong rotation direction, a log base mix-up) fails at least one of them.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.special as sps
+
+import oracle
+from oracle import (CONTIGUOUS, STRIPED, ZIGZAG, causal_pair_counts, full_attention,
+                    full_attention_rows, layout_positions, merge_partials, ring_partials,
+                    ring_sim, tile_classes_bruteforce, tile_counts)
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# Layouts and causal pair counts
+# ---------------------------------------------------------------------------
+
+def test_printed_causal_pair_counts(golden_dir):
+    g = _load(golden_dir, "causal_pair_counts.json")
+    c = causal_pair_counts(g["num_devices"], g["block_size"], CONTIGUOUS)
+    s = causal_pair_counts(g["num_devices"], g["block_size"], STRIPED)
+    assert c["work"] == g["contiguous"]["work"]
+    assert s["work"] == g["striped"]["work"]
+    assert f"{c['imbalance']:.2f}" == g["contiguous"]["imbalance_2dp"]
+    assert f"{s['imbalance']:.2f}" == g["striped"]["imbalance_2dp"]
+    assert (c["total"] == s["total"]) is g["same_total"]
+
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+@pytest.mark.parametrize("seq,n", [(8, 2), (12, 4), (128, 8), (4096, 32), (96, 8)])
+def test_layout_is_a_permutation(layout, seq, n):
+    if layout == ZIGZAG and seq % (2 * n):
+        pytest.skip("zigzag needs 2N | S")
+    pos = layout_positions(layout, seq, n)
+    assert sorted(pos.tolist()) == list(range(seq))
+    s_n = seq // n
+    for p in range(n):   # positions increase inside every shard
+        assert np.all(np.diff(pos[p * s_n:(p + 1) * s_n]) > 0)
+
+
+def test_layout_small_tables():
+    # written out by hand from the three definitions
+    assert layout_positions(CONTIGUOUS, 8, 2).tolist() == [0, 1, 2, 3, 4, 5, 6, 7]
+    assert layout_positions(STRIPED, 8, 2).tolist() == [0, 2, 4, 6, 1, 3, 5, 7]
+    assert layout_positions(ZIGZAG, 8, 2).tolist() == [0, 1, 6, 7, 2, 3, 4, 5]
+    z = layout_positions(ZIGZAG, 12, 3)      # chunks of 2: p0={0,1,10,11}
+    assert z[:4].tolist() == [0, 1, 10, 11]
+    assert z[4:8].tolist() == [2, 3, 8, 9]
+    assert z[8:].tolist() == [4, 5, 6, 7]
+
+
+def test_zigzag_exact_balance():
+    for n, blk in [(8, 16), (4, 8), (2, 64)]:
+        z = causal_pair_counts(n, blk, ZIGZAG)
+        assert len(set(z["work"])) == 1
+        assert z["total"] == n * blk * (n * blk + 1) // 2
+
+
+def test_layout_rejects_uneven():
+    with pytest.raises(ValueError):
+        layout_positions(CONTIGUOUS, 10, 4)
+    with pytest.raises(ValueError):
+        layout_positions(ZIGZAG, 12, 4)
+
+
+# ---------------------------------------------------------------------------
+# Plain attention
+# ---------------------------------------------------------------------------
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def test_full_attention_matches_scipy():
+    q, k, v = _rand((1, 2, 20, 8), 1), _rand((1, 2, 20, 8), 2), _rand((1, 2, 20, 8), 3)
+    o, lse = full_attention(q, k, v)
+    for h in range(2):
+        s = q[0, h] @ k[0, h].T / np.sqrt(8)
+        np.testing.assert_allclose(o[0, h], sps.softmax(s, axis=1) @ v[0, h], atol=1e-13)
+        np.testing.assert_allclose(lse[0, h], sps.logsumexp(s, axis=1), atol=1e-13)
+
+
+def test_full_attention_causal_matches_scipy():
+    q, k, v = _rand((1, 1, 17, 4), 4), _rand((1, 1, 17, 4), 5), _rand((1, 1, 17, 4), 6)
+    o, lse = full_attention(q, k, v, causal=True, scale=0.3)
+    s = q[0, 0] @ k[0, 0].T * 0.3
+    s[np.triu_indices(17, 1)] = -np.inf
+    np.testing.assert_allclose(o[0, 0], sps.softmax(s, axis=1) @ v[0, 0], atol=1e-13)
+    np.testing.assert_allclose(lse[0, 0], sps.logsumexp(s, axis=1), atol=1e-13)
+    # causal row 0 sees only key 0
+    np.testing.assert_allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0, 0], 0.3 * q[0, 0, 0] @ k[0, 0, 0], atol=1e-14)
+
+
+def test_full_attention_closed_forms():
+    d = 16
+    q = _rand((1, 1, 5, d), 7)
+    kv = _rand((1, 1, 1, d), 8)
+    k = np.repeat(kv, 9, axis=2)                # 9 identical keys
+    v = _rand((1, 1, 9, d), 9)
+    o, lse = full_attention(q, k, v)
+    np.testing.assert_allclose(o[0, 0], np.repeat(v[0, 0].mean(0, keepdims=True), 5, 0), atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], np.log(9) + (q[0, 0] @ kv[0, 0, 0]) / np.sqrt(d), atol=1e-13)
+
+
+def test_full_attention_rows_sum_to_one():
+    q, k = _rand((1, 1, 30, 8), 10), _rand((1, 1, 30, 8), 11)
+    eye = np.eye(30)[None, None]                 # V = identity exposes the probabilities
+    vv = np.zeros((1, 1, 30, 30)); vv[:] = eye
+    qq = np.concatenate([q, np.zeros((1, 1, 30, 22))], axis=3)
+    kk = np.concatenate([k, np.zeros((1, 1, 30, 22))], axis=3)
+    for causal in (False, True):
+        o, _ = full_attention(qq, kk, vv, causal=causal, scale=1 / np.sqrt(8))
+        np.testing.assert_allclose(o[0, 0].sum(1), 1.0, atol=1e-14)
+        assert np.all(o >= 0)
+
+
+def test_gqa_head_mapping():
+    q = _rand((2, 6, 11, 4), 12)
+    k, v = _rand((2, 3, 11, 4), 13), _rand((2, 3, 11, 4), 14)
+    o, lse = full_attention(q, k, v, causal=True)
+    for b in range(2):
+        for h in range(6):
+            g = h // 2
+            o1, l1 = full_attention(q[b:b + 1, h:h + 1], k[b:b + 1, g:g + 1], v[b:b + 1, g:g + 1], causal=True)
+            np.testing.assert_allclose(o[b, h], o1[0, 0], atol=1e-15)
+            np.testing.assert_allclose(lse[b, h], l1[0, 0], atol=1e-15)
+
+
+def test_full_attention_rows_equals_full():
+    q = _rand((1, 4, 40, 8), 15)
+    k, v = _rand((1, 2, 40, 8), 16), _rand((1, 2, 40, 8), 17)
+    pos = layout_positions(ZIGZAG, 40, 4)
+    o, lse = full_attention(q, k, v, causal=True, positions=pos)
+    picks = [(0, h, r) for h in range(4) for r in (0, 1, 9, 10, 22, 39)]
+    o2, l2 = full_attention_rows(q, k, v, picks, causal=True, positions=pos, chunk=5)
+    for n, (b, h, r) in enumerate(picks):
+        np.testing.assert_allclose(o2[n], o[b, h, r], atol=1e-14)
+        np.testing.assert_allclose(l2[n], lse[b, h, r], atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# The ring
+# ---------------------------------------------------------------------------
+
+def test_toy_ring_equals_attention(golden_dir):
+    g = _load(golden_dir, "toy_ring.json")
+    n, blk, d = g["n_devices"], g["tokens_per_device"], g["head_dim"]
+    rng = np.random.default_rng(1)
+    Q, K, V = (rng.normal(size=(n * blk, d)) for _ in range(3))
+    o, lse = ring_sim(Q[None, None], K[None, None], V[None, None], n)
+    s = Q @ K.T / np.sqrt(d)
+    ref = sps.softmax(s, axis=1) @ V
+    assert np.allclose(o[0, 0], ref)                      # the page's own check
+    np.testing.assert_allclose(o[0, 0], ref, atol=1e-13)
+    np.testing.assert_allclose(lse[0, 0], sps.logsumexp(s, axis=1), atol=1e-13)
+
+
+def test_module23_example(golden_dir):
+    torch = pytest.importorskip("torch")
+    g = _load(golden_dir, "module23_exact.json")
+    torch.manual_seed(0)
+    q, k, v = (torch.randn(*g["shape_bhsd"]) for _ in range(3))
+    q, k, v = q.double().numpy(), k.double().numpy(), v.double().numpy()
+    d = q.shape[-1]
+    ring, _ = ring_sim(q, k, v, g["num_devices"])
+    s = q @ np.swapaxes(k, -1, -2) / np.sqrt(d)
+    ref = sps.softmax(s, axis=-1) @ v
+    assert np.abs(ring - ref).max() <= g["atol"]
+    tri = np.triu(np.ones((96, 96), bool), 1)
+    ref_c = sps.softmax(np.where(tri, np.finfo(np.float64).min, s), axis=-1) @ v
+    ring_c, _ = ring_sim(q, k, v, g["num_devices"], causal=True)
+    assert np.abs(ring_c - ref_c).max() <= g["atol"]
+    np.testing.assert_allclose(ring_c, ref_c, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+def test_ring_layout_invariance(layout):
+    # natural-order inputs, permuted into the layout, ringed, then un-permuted
+    B, Hq, Hkv, S, d, n = 1, 4, 2, 48, 8, 4
+    q, k, v = _rand((B, Hq, S, d), 20), _rand((B, Hkv, S, d), 21), _rand((B, Hkv, S, d), 22)
+    pos = layout_positions(layout, S, n)
+    o_ref, l_ref = full_attention(q, k, v, causal=True)
+    o_l, l_l = ring_sim(q[:, :, pos], k[:, :, pos], v[:, :, pos], n, positions=pos, causal=True)
+    back_o = np.empty_like(o_l); back_o[:, :, pos] = o_l
+    back_l = np.empty_like(l_l); back_l[:, :, pos] = l_l
+    np.testing.assert_allclose(back_o, o_ref, atol=1e-13)
+    np.testing.assert_allclose(back_l, l_ref, atol=1e-13)
+
+
+def test_ring_one_shard_is_attention():
+    q, k, v = _rand((1, 2, 9, 4), 23), _rand((1, 1, 9, 4), 24), _rand((1, 1, 9, 4), 25)
+    for causal in (False, True):
+        a = ring_sim(q, k, v, 1, causal=causal)
+        b = full_attention(q, k, v, causal=causal)
+        np.testing.assert_allclose(a[0], b[0], atol=1e-14)
+        np.testing.assert_allclose(a[1], b[1], atol=1e-14)
+
+
+def test_ring_large_logits():
+    # Q scaled so the running max moves a lot between blocks
+    q = 4 * _rand((1, 1, 64, 16), 26)
+    k, v = _rand((1, 1, 64, 16), 27), _rand((1, 1, 64, 16), 28)
+    for causal in (False, True):
+        a = ring_sim(q, k, v, 8, causal=causal, scale=1.0)
+        b = full_attention(q, k, v, causal=causal, scale=1.0)
+        np.testing.assert_allclose(a[0], b[0], atol=1e-12)
+        np.testing.assert_allclose(a[1], b[1], rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Partials and merging
+# ---------------------------------------------------------------------------
+
+def test_merge_of_halves_is_attention():
+    q = _rand((1, 2, 10, 8), 30)
+    k, v = _rand((1, 2, 14, 8), 31), _rand((1, 2, 14, 8), 32)
+    oa, la = full_attention(q, k[:, :, :5], v[:, :, :5], scale=0.35)
+    ob, lb = full_attention(q, k[:, :, 5:], v[:, :, 5:], scale=0.35)
+    o, l = merge_partials(np.stack([oa, ob]), np.stack([la, lb]))
+    # single-call reference on all 14 keys (q and keys have different lengths)
+    s = np.einsum("bhqd,bhkd->bhqk", q, k) * 0.35
+    np.testing.assert_allclose(o, np.einsum("bhqk,bhkd->bhqd", sps.softmax(s, -1), v), atol=1e-14)
+    np.testing.assert_allclose(l, sps.logsumexp(s, -1), atol=1e-14)
+
+
+def test_merge_ignores_empty_parts():
+    o = _rand((3, 4, 6), 33)
+    l = _rand((3, 4), 34)
+    l[1] = -np.inf
+    m1, l1 = merge_partials(o, l)
+    m2, l2 = merge_partials(o[[0, 2]], l[[0, 2]])
+    np.testing.assert_allclose(m1, m2, atol=1e-15)
+    np.testing.assert_allclose(l1, l2, atol=1e-15)
+    m3, l3 = merge_partials(o[:1], np.full((1, 4), -np.inf))
+    assert np.all(m3 == 0) and np.all(np.isneginf(l3))
+
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_partials_merge_to_ring(layout, causal):
+    B, Hq, Hkv, S, d, n = 1, 2, 1, 24, 4, 3
+    q, k, v = _rand((B, Hq, S, d), 40), _rand((B, Hkv, S, d), 41), _rand((B, Hkv, S, d), 42)
+    pos = layout_positions(layout, S, n)
+    op, lp = ring_partials(q, k, v, n, positions=pos, causal=causal)
+    o, l = merge_partials(op, lp)
+    o2, l2 = ring_sim(q, k, v, n, positions=pos, causal=causal)
+    np.testing.assert_allclose(o, o2, atol=1e-13)
+    np.testing.assert_allclose(l, l2, atol=1e-13)
+    # order independence: merging the steps in reverse order changes nothing
+    o3, l3 = merge_partials(op[::-1], lp[::-1])
+    np.testing.assert_allclose(o3, o2, atol=1e-13)
+    if causal and layout == CONTIGUOUS:
+        # shard 0 at step 1 holds the last block: strictly in the future
+        assert np.all(np.isneginf(lp[1, :, :, : S // n]))
+
+
+# ---------------------------------------------------------------------------
+# Tile classification
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+@pytest.mark.parametrize("seq,n,tile", [(96, 4, 8), (64, 4, 5), (120, 3, 16), (64, 8, 4)])
+def test_tile_counts_bruteforce(layout, seq, n, tile):
+    if layout == ZIGZAG and seq % (2 * n):
+        pytest.skip("zigzag needs 2N | S")
+    for causal in (True, False):
+        a = tile_counts(layout, seq, n, causal=causal, tile=tile)
+        b = tile_classes_bruteforce(layout, seq, n, causal=causal, tile=tile)
+        for x, y in zip(a, b):
+            assert x.tolist() == y.tolist()
+
+
+def test_tile_counts_unit_tiles_are_pair_counts(golden_dir):
+    # with 1x1 tiles, FULL counts are exactly the causal pairs of each device
+    g = _load(golden_dir, "causal_pair_counts.json")
+    for layout in (CONTIGUOUS, STRIPED):
+        full, part, skip = tile_counts(layout, 128, 8, causal=True, tile=1)
+        assert full.tolist() == g[layout]["work"]
+        assert part.sum() == 0
+        assert (full + skip).tolist() == [128 * 16] * 8
+
+
+def test_tile_counts_closed_forms_seq32k():
+    # 32768 tokens, 8 shards, 128x128 tiles: global tile a meets tiles b<a FULL,
+    # b=a PARTIAL, b>a SKIP (both layouts keep tiles 128-aligned in position)
+    full, part, skip = tile_counts(CONTIGUOUS, 32768, 8)
+    for p in range(8):
+        assert (full[p], part[p], skip[p]) == (1024 * p + 496, 32, 1024 * (7 - p) + 496)
+    full, part, skip = tile_counts(ZIGZAG, 32768, 8)
+    assert full.tolist() == [4080] * 8 and part.tolist() == [32] * 8 and skip.tolist() == [4080] * 8
+
+
+def test_tile_counts_closed_forms_striped_131k():
+    full, part, skip = tile_counts(STRIPED, 131072, 32)
+    assert full.tolist() == [32 * 496] * 32
+    assert part.tolist() == [32 * 32] * 32
+    assert skip.tolist() == [32 * 496] * 32
+
+
+def test_oracle_exports():
+    for name in oracle.__all__:
+        assert hasattr(oracle, name)
