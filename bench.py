@@ -1,0 +1,338 @@
+"""Benchmark of the ring-attention forward on GB300 (one JSON line on stdout).
+
+A step is one pass of the whole path over one batch of synthetic input that is
+already resident in HBM: natural-order Q, K, V are moved into the ring layout
+(ra_layout_perm), the ring forward runs (ra_fwd, fused O and LSE), and O and
+LSE are moved back to natural order.  Default workload: causal zigzag, 1,048,576
+tokens in 8 shards, batch 1, 32 query / 8 key-value heads, d = 128, bf16.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload on the host cores (the only other place this script runs the oracle).
+Under torchrun each rank runs an independent replica (no data-path collective);
+rank 0 prints max-over-ranks timing.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-attention fwd TFLOP/s (bf16, 1 GB300) and % of dense tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def cpu_oracle_sample(wl, rows=192, seed=11):
+    """Time the float64 oracle on `rows` causal query rows of one key/value head.
+
+    Inputs are host-drawn N(0,1) of the workload's shape (one kv head, rows of its
+    query heads at uniformly drawn positions); returns (TFLOP/s, seconds, flops, desc).
+    """
+    import oracle
+    rng = np.random.default_rng(seed)
+    S, d = wl.seq, wl.head_dim
+    k = rng.standard_normal((S, d))
+    v = rng.standard_normal((S, d))
+    pos_all = oracle.layout_positions(wl.layouts[0], S, wl.n_shards)
+    qpos = np.sort(rng.choice(S, size=rows, replace=False))
+    q = rng.standard_normal((rows, d))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k[pos_all], v[pos_all], q_positions=qpos, k_positions=pos_all,
+                          causal=wl.causal)
+    dt = time.perf_counter() - t0
+    keys = (qpos + 1) if wl.causal else np.full(rows, S)
+    flops = 4.0 * d * float(keys.sum())
+    desc = (f"{rows} query rows (uniform positions, seed {seed}) of one head against all {S} keys "
+            f"of the {wl.name} workload, float64 numpy oracle")
+    return flops / dt / 1e12, dt, flops, desc
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    times, tf = [], []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        v, dt, flops, desc = cpu_oracle_sample(wl, rows=args.ref_rows, seed=100 + i)
+        if i >= args.warmup:
+            times.append(dt)
+            tf.append(v)
+    value = statistics.median(tf)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl):
+    return {"workload": wl.name, "batch": wl.batch, "seq": wl.seq, "heads_q": wl.heads_q,
+            "heads_kv": wl.heads_kv, "head_dim": wl.head_dim, "n_shards": wl.n_shards,
+            "layout": wl.layouts[0], "causal": wl.causal,
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
+# ------------------------------------------------------------- GPU (ours) --
+
+def run_ours(args, wl):
+    import torch
+    import context_ring_attention_gb300 as ra
+    from context_ring_attention_gb300 import workloads
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        pg = dist
+    dev = torch.device("cuda", local)
+    layout = wl.layouts[0]
+    N = wl.n_shards
+    plan = ra.ra_plan(wl.batch, wl.seq, wl.heads_q, wl.heads_kv, wl.head_dim, N, layout, wl.causal, wl.dtype)
+    q, k, v = workloads.torch_inputs(wl, dev)
+    ql, kl, vl = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    o_l = torch.empty_like(q)
+    lse_l = torch.empty((wl.batch, wl.heads_q, wl.seq), dtype=torch.float32, device=dev)
+    o_n = torch.empty_like(q)
+    lse_n = torch.empty_like(lse_l)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 6
+
+    def step(fwd_events=None):
+        ra.ra_layout_perm(q, layout, N, out=ql)
+        ra.ra_layout_perm(k, layout, N, out=kl)
+        ra.ra_layout_perm(v, layout, N, out=vl)
+        if fwd_events is not None:
+            fwd_events[0].record(stream)
+        ra.ra_fwd(plan, ql, kl, vl, o=o_l, lse=lse_l)
+        if fwd_events is not None:
+            fwd_events[1].record(stream)
+        ra.ra_layout_perm(o_l, layout, N, inverse=True, out=o_n)
+        ra.ra_layout_perm(lse_l, layout, N, inverse=True, out=lse_n)
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    ra.ra_sync_status(plan)
+
+    fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(fwd_ev[i])
+        end.record(stream)
+        barrier()
+    ra.ra_sync_status(plan)
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    if pg is not None:
+        t = torch.tensor([total_ms, max(fwd_ms)], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms, fwd_max = t.tolist()
+    ms_per_step = total_ms / args.steps
+    flops = wl.flops()
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # End to end through host buffers: H2D of natural-order Q/K/V, the step, D2H of O/LSE.
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+        ho = torch.empty(o_n.shape, dtype=o_n.dtype, pin_memory=True)
+        hl = torch.empty(lse_n.shape, dtype=lse_n.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(o_n, non_blocking=True)
+            hl.copy_(lse_n, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1) / args.steps
+        if pg is not None:
+            t = torch.tensor([e_ms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e_ms = t.item()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        ra.ra_sync_status(plan)
+
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return 0
+
+    peaks, src = load_peaks()
+    fwd_mean = statistics.mean(fwd_ms)
+    achieved = flops / (fwd_mean * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = None
+    tf_path = os.path.join(ROOT, "profiles", "fwd_bf16_traffic.json")
+    if os.path.exists(tf_path):
+        try:
+            with open(tf_path) as f:
+                rec = json.load(f)
+            if rec.get("workload") == wl.name:
+                traffic = rec.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+    full, part, skip = ra.ra_plan_tile_counts(plan)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(wl),
+        "roofline": {"bound": "tensor", "kernel": "fwd_bf16_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{src} bf16_tflops_sustained",
+                     "frac_of_burst": achieved / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                     "fwd_ms_mean": fwd_mean},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "tile_counts": {"full": full.tolist(), "partial": part.tolist(), "skip": skip.tolist(),
+                        "granularity": "128x128 per (batch, query head)"},
+        "algorithmic_flops_per_step": flops,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        v_cpu, dt, _, desc = cpu_oracle_sample(wl, rows=args.ref_rows)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="zigzag_1m_n8")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=192)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from context_ring_attention_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

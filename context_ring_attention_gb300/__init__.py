@@ -1,0 +1,240 @@
+"""GB300 ring-attention forward: Python binding of libra.so (include/ra.h).
+
+The functions keep the C names (``ra_plan``, ``ra_fwd``, ``ra_merge_partials``,
+``ra_layout_perm``, ``ra_layout_index``, ``ra_plan_tile_counts``,
+``ra_sync_status``, ``ra_last_error``).  This module only marshals arguments:
+PyTorch supplies device memory and the current stream, every step of the
+computation runs in the library's CUDA kernels, and there is no fallback -- if
+libra.so is missing or cannot be loaded, every call raises.
+
+Tensors are ``[B, H, S, d]`` contiguous with S in layout order (shard p owns rows
+[p*S/N, (p+1)*S/N)); ``ra_layout_perm`` moves natural order <-> layout order.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "RaError", "Plan", "LAYOUTS",
+    "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
+    "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error",
+    "library_path", "load_library", "EXPORTED",
+]
+
+LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
+DTYPES = {"f32": 0, "bf16": 1}
+_STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
+           4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
+EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
+            "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+class RaError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        self.name = _STATUS.get(status, str(status))
+        super().__init__(f"{self.name}: {message}")
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seq", ctypes.c_int64), ("heads_q", ctypes.c_int32),
+                ("heads_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("n_shards", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("causal", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+def library_path():
+    return os.path.join(_HERE, "libra.so")
+
+
+def load_library():
+    """Load libra.so (built in-tree by ``build.build()``); raises if it is absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run context_ring_attention_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, VP = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    sig = {
+        "ra_plan": ([ctypes.POINTER(_Problem), ctypes.POINTER(P)], I32),
+        "ra_plan_destroy": ([P], I32),
+        "ra_plan_tile_counts": ([P, VP, VP, VP], I32),
+        "ra_fwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP], I32),
+        "ra_merge_partials": ([I32, I64, I32, VP, VP, VP, I32, VP, VP], I32),
+        "ra_layout_perm": ([I32, I64, I32, I32, I64, I32, VP, VP, VP], I32),
+        "ra_layout_index": ([I32, I64, I32, VP], I32),
+        "ra_sync_status": ([P, VP], I32),
+        "ra_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _LIB = lib
+    return lib
+
+
+def ra_last_error():
+    return load_library().ra_last_error().decode()
+
+
+def _check(status):
+    if status != 0:
+        raise RaError(status, ra_last_error())
+
+
+def _layout(layout):
+    return LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """Owns an ``ra_plan_t``; the problem it was built for is ``self.problem``."""
+
+    def __init__(self, handle, problem):
+        self._h = handle
+        self.problem = problem
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            load_library().ra_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def ra_plan(batch, seq, heads_q, heads_kv, head_dim, n_shards, layout="contiguous",
+            causal=False, dtype="bf16", scale=0.0):
+    """Validate a problem and build its ring schedule (see include/ra.h)."""
+    lib = load_library()
+    dt = DTYPES[dtype] if isinstance(dtype, str) else int(dtype)
+    prob = _Problem(int(batch), int(seq), int(heads_q), int(heads_kv), int(head_dim), int(n_shards),
+                    _layout(layout), int(bool(causal)), dt, float(scale or 0.0))
+    h = ctypes.c_void_p()
+    _check(lib.ra_plan(ctypes.byref(prob), ctypes.byref(h)))
+    info = dict(batch=int(batch), seq=int(seq), heads_q=int(heads_q), heads_kv=int(heads_kv),
+                head_dim=int(head_dim), n_shards=int(n_shards), layout=_layout(layout),
+                causal=bool(causal), dtype=dt, scale=float(scale or 0.0))
+    return Plan(h, info)
+
+
+def ra_plan_destroy(plan):
+    plan.close()
+
+
+def ra_plan_tile_counts(plan):
+    """Per-shard (FULL, PARTIAL, SKIP) tile counts of one (batch, query head)."""
+    n = plan.problem["n_shards"]
+    full, part, skip = (np.zeros(n, np.int64) for _ in range(3))
+    _check(load_library().ra_plan_tile_counts(plan.handle, full.ctypes.data, part.ctypes.data,
+                                              skip.ctypes.data))
+    return full, part, skip
+
+
+def ra_fwd(plan, q, k, v, o=None, lse=None, partials=False, o_parts=None, lse_parts=None,
+           stream=None):
+    """Ring-attention forward.  Fused: returns (O, LSE).  partials=True: (O_parts, LSE_parts)."""
+    import torch
+    pb = plan.problem
+    B, Hq, S, d, N = pb["batch"], pb["heads_q"], pb["seq"], pb["head_dim"], pb["n_shards"]
+    dt = torch.bfloat16 if pb["dtype"] == 1 else torch.float32
+    for name, t, heads in (("q", q, Hq), ("k", k, pb["heads_kv"]), ("v", v, pb["heads_kv"])):
+        if tuple(t.shape) != (B, heads, S, d) or t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {(B, heads, S, d)}")
+    lib = load_library()
+    if partials:
+        if o_parts is None:
+            o_parts = torch.empty((N, B, Hq, S, d), dtype=torch.float32, device=q.device)
+        if lse_parts is None:
+            lse_parts = torch.empty((N, B, Hq, S), dtype=torch.float32, device=q.device)
+        _check(lib.ra_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), None, None, _ptr(o_parts),
+                          _ptr(lse_parts), _stream(stream)))
+        return o_parts, lse_parts
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _check(lib.ra_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), None, None,
+                      _stream(stream)))
+    return o, lse
+
+
+def ra_merge_partials(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stream=None):
+    """Merge [n, ..., d] partial outputs with their [n, ...] LSEs -> (O, LSE)."""
+    import torch
+    n, d = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    if o_parts.dtype != torch.float32 or lse_parts.dtype != torch.float32:
+        raise ValueError("partials must be float32")
+    if not (o_parts.is_contiguous() and lse_parts.is_contiguous()):
+        raise ValueError("partials must be contiguous")
+    out_dtype = out_dtype or torch.float32
+    if o is None:
+        o = torch.empty(o_parts.shape[1:], dtype=out_dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    code = 1 if o.dtype == torch.bfloat16 else 0
+    _check(load_library().ra_merge_partials(n, rows, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o), code,
+                                            _ptr(lse), _stream(stream)))
+    return o, lse
+
+
+def ra_layout_perm(x, layout, n_shards, inverse=False, seq_dim=None, out=None, stream=None):
+    """Natural -> layout order (inverse=False) or back, along ``seq_dim``.
+
+    ``seq_dim`` defaults to -2 for tensors of 3+ dims ([..., S, d]) and -1 otherwise
+    ([..., S], e.g. an LSE).  Everything after the sequence axis moves as one row.
+    """
+    import torch
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if seq_dim is None:
+        seq_dim = -2 if x.dim() >= 3 else -1
+    seq_dim = seq_dim % x.dim()
+    seq = x.shape[seq_dim]
+    outer = int(np.prod(x.shape[:seq_dim], dtype=np.int64)) if seq_dim else 1
+    row_bytes = int(np.prod(x.shape[seq_dim + 1:], dtype=np.int64)) * x.element_size()
+    if out is None:
+        out = torch.empty_like(x)
+    _check(load_library().ra_layout_perm(_layout(layout), seq, int(n_shards), int(bool(inverse)), outer,
+                                         row_bytes, _ptr(x), _ptr(out), _stream(stream)))
+    return out
+
+
+def ra_layout_index(layout, seq, n_shards):
+    """Natural position of every layout-ordered row (host helper)."""
+    pos = np.zeros(int(seq), np.int64)
+    _check(load_library().ra_layout_index(_layout(layout), int(seq), int(n_shards), pos.ctypes.data))
+    return pos
+
+
+def ra_sync_status(plan, stream=None):
+    """Synchronize the stream and raise RaError if a device wait of this plan timed out."""
+    _check(load_library().ra_sync_status(plan.handle, _stream(stream)))

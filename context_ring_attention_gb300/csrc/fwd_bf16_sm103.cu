@@ -1,0 +1,595 @@
+// Ring-attention forward, bf16, d = 128, on the sm_100-family tensor cores.
+//
+// What it computes: for every query row of shard p, the online-softmax fold of
+// Module 23, "The Math: One Block at a Time" over the key/value blocks of shards
+// (p - t) mod N for ring steps t = 0..N-1 (the rotation of "3.6 Distributed
+// Training II", section "Ring Attention"), finished as O = o / l; causal blocks
+// strictly in the future are skipped and the rest masked by global position
+// (Module 23, "Exact by Construction").  One GPU plays all N devices: the ring
+// rotation is the order in which each query tile visits key tiles.
+//
+// How (one persistent CTA per SM, 12 warps):
+//   warp 0     TMA producer: Q tiles once per work item, then K and V tiles in
+//              ring order into a 3-slot shared-memory ring (128B swizzle).
+//   warp 1     tcgen05 issuer: S = Q K^T into TMEM, O += P V into TMEM.
+//   warps 4-7  softmax for query tile 0, warps 8-11 for query tile 1: one thread
+//              per row reads S from TMEM, updates m and l, writes P (bf16) to
+//              shared memory, rescales O in TMEM when m moves, and writes O / l
+//              and the LSE at the end of a segment.
+// Two query tiles per CTA let one tile's softmax overlap the other tile's MMAs.
+// TMEM: S0 cols 0-127, S1 128-255, O0 256-383, O1 384-511 (all 512 columns).
+//
+// Every mbarrier wait is bounded (~1 s).  On expiry the CTA raises an abort flag,
+// records the role in the plan's status word, drains its own in-flight TMA
+// loads and MMAs (bounded again), frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ra_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
+constexpr uint32_t kHalfBytes = 128 * 64 * 2;   // 128 rows x one 128-byte swizzle column
+constexpr int kStages = 3;
+constexpr uint32_t kOffQ = 0;                            // Q0, Q1
+constexpr uint32_t kOffKV = 2 * kTileBytes;              // K/V ring
+constexpr uint32_t kOffP = kOffKV + kStages * kTileBytes;  // P0, P1
+constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+
+enum : int {
+  kQFull = 0,
+  kQEmpty = 1,
+  kKVFull = 2,
+  kKVEmpty = kKVFull + kStages,
+  kSFull = kKVEmpty + kStages,
+  kPFull = kSFull + 2,
+  kOFull = kPFull + 2,
+  kDone = kOFull + 2,
+  kNumBars = kDone + 1
+};
+constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base written by tcgen05.alloc
+constexpr uint32_t kOffAbort = kOffSlot + 4;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + slack to align the base to 1 KiB
+static_assert(8 * kNumBars + 8 <= 256, "barrier area");
+
+constexpr uint32_t kTmemCols = 512;
+__device__ __forceinline__ uint32_t col_s(int g) { return g ? 128u : 0u; }
+__device__ __forceinline__ uint32_t col_o(int g) { return g ? 384u : 256u; }
+
+constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 128, false, true);  // V is MN-major
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;
+constexpr float kRescaleSlack = 8.0f;  // log2 units: keep a stale max while p <= 2^8
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Ctl {
+  uint32_t bars;
+  volatile uint32_t* abort;
+  uint32_t* status;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * (uint32_t)i; }
+};
+
+// Bounded wait for phase `parity` of a barrier; false on abort or expiry.
+__device__ __noinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t parity, uint32_t who) {
+  if (ptx::mbar_test(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_test(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*c.abort) return false;
+      if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
+        *c.abort = 1u;
+        atomicOr(c.status, who);
+        return false;
+      }
+    }
+  }
+}
+
+// Teardown wait: ignores the abort flag, still bounded.
+__device__ __noinline__ void drain_bar(const Ctl& c, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (!ptx::mbar_test(bar, parity)) {
+    if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
+      atomicOr(c.status, kStatusTimeoutTeardown);
+      return;
+    }
+  }
+}
+
+// Position in the virtual ring: step t, key shard r, key tile kt of nt.
+struct Walk {
+  int t, r, kt, nt;
+};
+
+__device__ __forceinline__ void walk_to_next_step(Walk& w, const FwdParams& P, int p, int64_t maxq) {
+  for (++w.t; w.t < P.n_shards; ++w.t) {
+    w.r = (p - w.t + P.n_shards) % P.n_shards;
+    w.nt = visit_tiles(P.layout, P.n_shards, P.s_n, P.causal, w.r, maxq);
+    if (w.nt > 0) {
+      w.kt = 0;
+      return;
+    }
+  }
+}
+__device__ __forceinline__ void walk_begin(Walk& w, const FwdParams& P, int p, int64_t maxq) {
+  w.t = -1;
+  w.kt = 0;
+  w.nt = 0;
+  walk_to_next_step(w, P, p, maxq);
+}
+__device__ __forceinline__ void walk_advance(Walk& w, const FwdParams& P, int p, int64_t maxq) {
+  if (++w.kt >= w.nt) walk_to_next_step(w, P, p, maxq);
+}
+
+// ------------------------------------------------------------------ producer --
+struct ProducerState {
+  uint32_t kv_issued;
+  uint32_t q_issued;
+};
+
+__device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase,
+                             const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                             ProducerState& st) {
+  uint32_t kv_it = 0, u = 0;
+  for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x, ++u) {
+    const WorkItem it = P.items[idx];
+    if (!wait_bar(c, c.bar(kQEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer)) break;
+    const bool two = it.bh1 >= 0;
+    ptx::mbar_arrive_expect_tx(c.bar(kQFull), (two ? 2u : 1u) * kTileBytes);
+    const int32_t y0 = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
+    ptx::tma_load_2d(sbase + kOffQ, tq, c.bar(kQFull), 0, y0);
+    ptx::tma_load_2d(sbase + kOffQ + kHalfBytes, tq, c.bar(kQFull), 64, y0);
+    if (two) {
+      const int32_t y1 = (int32_t)((int64_t)it.bh1 * P.seq + (int64_t)it.shard * P.s_n + it.row1);
+      ptx::tma_load_2d(sbase + kOffQ + kTileBytes, tq, c.bar(kQFull), 0, y1);
+      ptx::tma_load_2d(sbase + kOffQ + kTileBytes + kHalfBytes, tq, c.bar(kQFull), 64, y1);
+    }
+    st.q_issued = u + 1;
+    const int b = it.bh0 / P.heads_q;
+    const int kvh = (it.bh0 % P.heads_q) / P.group;
+    const int64_t kv_base = (int64_t)(b * P.heads_kv + kvh) * P.seq;
+    Walk w;
+    walk_begin(w, P, it.shard, it.maxq);
+    bool ok = true;
+    while (ok && w.t < P.n_shards) {
+      const int32_t y = (int32_t)(kv_base + (int64_t)w.r * P.s_n + (int64_t)w.kt * kTileRows);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // K tile, then V tile
+        const uint32_t s = kv_it % kStages, use = kv_it / kStages;
+        if (!wait_bar(c, c.bar(kKVEmpty + s), (use & 1u) ^ 1u, kStatusTimeoutProducer)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = sbase + kOffKV + s * kTileBytes;
+        const CUtensorMap* map = which ? tv : tk;
+        ptx::mbar_arrive_expect_tx(c.bar(kKVFull + s), kTileBytes);
+        ptx::tma_load_2d(dst, map, c.bar(kKVFull + s), 0, y);
+        ptx::tma_load_2d(dst + kHalfBytes, map, c.bar(kKVFull + s), 64, y);
+        st.kv_issued = ++kv_it;
+      }
+      walk_advance(w, P, it.shard, it.maxq);
+    }
+    if (!ok) break;
+  }
+}
+
+// ----------------------------------------------------------------------- MMA --
+__device__ __forceinline__ void issue_s(uint32_t sbase, uint32_t tmem, int g, uint32_t ks) {
+  const uint32_t a0 = sbase + kOffQ + (uint32_t)g * kTileBytes;
+  const uint32_t b0 = sbase + kOffKV + ks * kTileBytes;
+#pragma unroll
+  for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of K = 16 over d = 128
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3u) * 32u;
+    ptx::mma_bf16_ss(tmem + col_s(g), ptx::sw128_desc(a0 + off, 16, 1024),
+                     ptx::sw128_desc(b0 + off, 16, 1024), kIdescS, kk > 0);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t sbase, uint32_t tmem, int g, uint32_t vs,
+                                         bool accumulate) {
+  const uint32_t a0 = sbase + kOffP + (uint32_t)g * kTileBytes;
+  const uint32_t b0 = sbase + kOffKV + vs * kTileBytes;
+#pragma unroll
+  for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of 16 keys
+    const uint32_t a_off = (kk >> 2) * kHalfBytes + (kk & 3u) * 32u;
+    // V is [keys][d]: 16 keys = 2 groups of 8 rows (SBO 1 KiB); d halves 16 KiB apart (LBO).
+    ptx::mma_bf16_ss(tmem + col_o(g), ptx::sw128_desc(a0 + a_off, 16, 1024),
+                     ptx::sw128_desc(b0 + kk * 2048u, kHalfBytes, 1024), kIdescPV,
+                     (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+__device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32_t tmem) {
+  const bool partials = P.o_parts != nullptr;
+  uint32_t kv_it = 0, u = 0, pj0 = 0, pj1 = 0;
+  for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x, ++u) {
+    const WorkItem it = P.items[idx];
+    const bool two = it.bh1 >= 0;
+    if (!wait_bar(c, c.bar(kQFull), u & 1u, kStatusTimeoutMma)) return;
+    ptx::tc_fence_after();
+    Walk cur;
+    walk_begin(cur, P, it.shard, it.maxq);
+    if (cur.t >= P.n_shards) {
+      ptx::mma_commit(c.bar(kQEmpty));
+      continue;
+    }
+    uint32_t ks = kv_it % kStages;
+    if (!wait_bar(c, c.bar(kKVFull + ks), (kv_it / kStages) & 1u, kStatusTimeoutMma)) return;
+    ptx::tc_fence_after();
+    issue_s(sbase, tmem, 0, ks);
+    ptx::mma_commit(c.bar(kSFull + 0));
+    if (two) {
+      issue_s(sbase, tmem, 1, ks);
+      ptx::mma_commit(c.bar(kSFull + 1));
+    }
+    ptx::mma_commit(c.bar(kKVEmpty + ks));
+    ++kv_it;
+    bool first_tile = true;
+    for (;;) {
+      Walk nxt = cur;
+      walk_advance(nxt, P, it.shard, it.maxq);
+      const bool has_next = nxt.t < P.n_shards;
+      const bool seg_first = partials ? (cur.kt == 0) : first_tile;
+      const bool seg_last = partials ? (!has_next || nxt.t != cur.t) : !has_next;
+      const uint32_t vs = kv_it % kStages;
+      if (!wait_bar(c, c.bar(kKVFull + vs), (kv_it / kStages) & 1u, kStatusTimeoutMma)) return;
+      ++kv_it;
+      if (!wait_bar(c, c.bar(kPFull + 0), pj0 & 1u, kStatusTimeoutMma)) return;
+      ++pj0;
+      ptx::tc_fence_after();
+      issue_pv(sbase, tmem, 0, vs, !seg_first);
+      if (seg_last) ptx::mma_commit(c.bar(kOFull + 0));
+      uint32_t ks2 = 0;
+      if (has_next) {
+        ks2 = kv_it % kStages;
+        if (!wait_bar(c, c.bar(kKVFull + ks2), (kv_it / kStages) & 1u, kStatusTimeoutMma)) return;
+        ptx::tc_fence_after();
+        issue_s(sbase, tmem, 0, ks2);
+        ptx::mma_commit(c.bar(kSFull + 0));
+      }
+      if (two) {
+        if (!wait_bar(c, c.bar(kPFull + 1), pj1 & 1u, kStatusTimeoutMma)) return;
+        ++pj1;
+        ptx::tc_fence_after();
+        issue_pv(sbase, tmem, 1, vs, !seg_first);
+        if (seg_last) ptx::mma_commit(c.bar(kOFull + 1));
+      }
+      ptx::mma_commit(c.bar(kKVEmpty + vs));
+      if (!has_next) break;
+      if (two) {
+        issue_s(sbase, tmem, 1, ks2);
+        ptx::mma_commit(c.bar(kSFull + 1));
+      }
+      ptx::mma_commit(c.bar(kKVEmpty + ks2));
+      ++kv_it;
+      cur = nxt;
+      first_tile = false;
+    }
+    ptx::mma_commit(c.bar(kQEmpty));
+  }
+}
+
+// ------------------------------------------------------------------- softmax --
+__device__ __forceinline__ void store_segment(const FwdParams& P, uint32_t tO, float m, float l,
+                                              bool valid, int64_t out_row, int t) {
+  const float inv = l > 0.f ? 1.0f / l : 0.f;
+  const float lse = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  const int64_t rows_all = (int64_t)P.batch * P.heads_q * P.seq;
+  if (P.o_parts != nullptr) {
+    float4* dst = reinterpret_cast<float4*>(P.o_parts + ((int64_t)t * rows_all + out_row) * 128);
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[32];
+      __syncwarp();
+      ptx::tmem_ld32(tO + cc * 32, v);
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[cc * 8 + q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                        __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+      }
+    }
+    if (valid) P.lse_parts[(int64_t)t * rows_all + out_row] = lse;
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(P.o) + out_row * 128);
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t v[32];
+      __syncwarp();
+      ptx::tmem_ld32(tO + cc * 32, v);
+      if (valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = ptx::pack_bf16x2(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                    __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+          dst[cc * 4 + q] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    if (valid && P.lse != nullptr) P.lse[out_row] = lse;
+  }
+}
+
+__device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32_t tmem, int g,
+                            int wq, int lane) {
+  const int row = wq * 32 + lane;
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  const uint32_t tS = tmem + lane_off + col_s(g);
+  const uint32_t tO = tmem + lane_off + col_o(g);
+  const uint32_t prow = sbase + kOffP + (uint32_t)g * kTileBytes + (uint32_t)row * 128u;
+  const uint32_t rsw = (uint32_t)row & 7u;
+  const bool partials = P.o_parts != nullptr;
+  const int N = P.n_shards;
+  const int64_t rows_all = (int64_t)P.batch * P.heads_q * P.seq;
+  const float sl2 = P.scale_log2;
+  uint32_t sj = 0, oj = 0;
+
+  for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x) {
+    const WorkItem it = P.items[idx];
+    if (g == 1 && it.bh1 < 0) continue;
+    const int bh = g ? it.bh1 : it.bh0;
+    const int p = it.shard;
+    const int64_t i = (int64_t)(g ? it.row1 : it.row0) + row;
+    const bool valid = i < P.s_n;
+    const int64_t my_pos = pos_of(P.layout, N, P.s_n, p, valid ? i : P.s_n - 1);
+    const int64_t out_row = (int64_t)bh * P.seq + (int64_t)p * P.s_n + i;
+    int last_t = -1;
+    for (int t = 0; t < N; ++t)
+      if (visit_tiles(P.layout, N, P.s_n, P.causal, (p - t + N) % N, it.maxq) > 0) last_t = t;
+
+    float m = -INFINITY, l = 0.f;
+    bool open = false;
+    for (int t = 0; t < N; ++t) {
+      const int r = (p - t + N) % N;
+      const int nt = visit_tiles(P.layout, N, P.s_n, P.causal, r, it.maxq);
+      if (nt == 0) {
+        if (partials && valid) {  // nothing of this block is causal for the tile
+          float4* dst = reinterpret_cast<float4*>(P.o_parts + ((int64_t)t * rows_all + out_row) * 128);
+          for (int q = 0; q < 32; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          P.lse_parts[(int64_t)t * rows_all + out_row] = -INFINITY;
+        }
+        continue;
+      }
+      const int64_t J = P.causal ? last_le(P.layout, N, P.s_n, r, my_pos) : P.s_n - 1;
+      for (int kt = 0; kt < nt; ++kt) {
+        const bool first = partials ? (kt == 0) : !open;
+        const bool last = partials ? (kt == nt - 1) : (t == last_t && kt == nt - 1);
+        open = true;
+        const int64_t j0 = (int64_t)kt * kTileRows;
+        int64_t lim = J - j0 + 1;
+        const int64_t cap = (P.s_n - j0 < kTileRows) ? P.s_n - j0 : kTileRows;
+        lim = lim < 0 ? 0 : (lim > cap ? cap : lim);
+        const int limit = (int)lim;
+
+        bool ok = wait_bar(c, c.bar(kSFull + g), sj & 1u, kStatusTimeoutSoftmax);
+        ++sj;
+        if (!__all_sync(0xffffffffu, ok)) return;
+        ptx::tc_fence_after();
+
+        // Pass 1: row max of the (masked) raw scores.
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          __syncwarp();
+          ptx::tmem_ld32(tS + cc * 32, v);
+          if (limit >= (cc + 1) * 32) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (cc * 32 + e < limit) mx = fmaxf(mx, __uint_as_float(v[e]));
+          }
+        }
+        const float mt = mx * sl2;  // in log2 units; -inf stays -inf
+        float m_new = m;
+        bool resc = false;
+        if (first) {
+          m_new = mt;
+          l = 0.f;
+        } else if (mt > m + kRescaleSlack) {
+          m_new = mt;
+          resc = true;
+        }
+        if (!first && __any_sync(0xffffffffu, resc)) {
+          // O and l were accumulated against the old max: bring them to the new one.
+          const float alpha = resc ? ptx::ex2_approx(m - m_new) : 1.0f;
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            __syncwarp();
+            ptx::tmem_ld32(tO + cc * 32, v);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            ptx::tmem_st32(tO + cc * 32, v);
+          }
+          l *= alpha;
+        }
+        m = m_new;
+        const float mref = (m == -INFINITY) ? 0.f : m;
+
+        // Pass 2: p = 2^(s*scale*log2e - m), row sum, P to shared memory as bf16.
+        float sum = 0.f;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          __syncwarp();
+          ptx::tmem_ld32(tS + cc * 32, v);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k0 = cc * 32 + 2 * e;
+            const float p0 = k0 < limit ? ptx::ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl2, -mref)) : 0.f;
+            const float p1 = k0 + 1 < limit ? ptx::ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -mref)) : 0.f;
+            sum += p0 + p1;
+            w[e] = ptx::pack_bf16x2(p0, p1);
+          }
+          const uint32_t line = prow + (uint32_t)(cc >> 1) * kHalfBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t chunk = (uint32_t)((cc & 1) * 4 + j);
+            ptx::st_shared_v4(line + ((chunk ^ rsw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
+        }
+        l += sum;
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(c.bar(kPFull + g));
+
+        if (last) {
+          ok = wait_bar(c, c.bar(kOFull + g), oj & 1u, kStatusTimeoutSoftmax);
+          ++oj;
+          if (!__all_sync(0xffffffffu, ok)) return;
+          ptx::tc_fence_after();
+          store_segment(P, tO, m, l, valid, out_row, t);
+          ptx::tc_fence_before();
+          m = -INFINITY;
+          l = 0.f;
+        }
+        __syncwarp();
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const FwdParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ctl c{sbase + kOffBar, reinterpret_cast<volatile uint32_t*>(sgen + kOffAbort), P.status};
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(c.bar(kQFull), 1);
+    ptx::mbar_init(c.bar(kQEmpty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(c.bar(kKVFull + s), 1);
+      ptx::mbar_init(c.bar(kKVEmpty + s), 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(c.bar(kSFull + g), 1);
+      ptx::mbar_init(c.bar(kPFull + g), 128);
+      ptx::mbar_init(c.bar(kOFull + g), 1);
+    }
+    ptx::mbar_init(c.bar(kDone), 1);
+    *c.abort = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tq);
+    ptx::tma_prefetch_desc(&tk);
+    ptx::tma_prefetch_desc(&tv);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + kOffSlot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + kOffSlot);
+
+  ProducerState ps{0u, 0u};
+  if (warp == 0) {
+    if (lane == 0) run_producer(P, c, sbase, &tq, &tk, &tv, ps);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      run_mma(P, c, sbase, tmem);
+      // Every MMA this thread issued must retire before TMEM is freed.
+      ptx::mma_commit(c.bar(kDone));
+      drain_bar(c, c.bar(kDone), 0);
+    }
+  } else if (warp >= 4) {
+    run_softmax(P, c, sbase, tmem, (warp - 4) >> 2, warp & 3, lane);
+  }
+
+  if (warp == 0 && lane == 0 && *c.abort) {
+    // Let this CTA's own TMA loads land before its shared memory goes away.
+    for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
+      if (ps.kv_issued > s) {
+        const uint32_t uses = (ps.kv_issued - 1 - s) / kStages + 1;  // loads issued to slot s
+        drain_bar(c, c.bar(kKVFull + s), (uses - 1) & 1u);
+      }
+    }
+    if (ps.q_issued > 0) drain_bar(c, c.bar(kQFull), (ps.q_issued - 1) & 1u);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [rows, 128] bf16 row-major, boxes of 128 rows x 64 columns, 128-byte swizzle.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128 * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int fwd_bf16_smem_bytes() { return (int)kSmemBytes; }
+
+cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, const void* v,
+                            int grid, cudaStream_t stream, const char** why) {
+  CUtensorMap tq, tk, tv;
+  const int64_t rows_q = (int64_t)prm.batch * prm.heads_q * prm.seq;
+  const int64_t rows_kv = (int64_t)prm.batch * prm.heads_kv * prm.seq;
+  if (!encode_rows(&tq, q, rows_q) || !encode_rows(&tk, k, rows_kv) || !encode_rows(&tv, v, rows_kv)) {
+    *why = "cuTensorMapEncodeTiled failed or is unavailable";
+    return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) {
+    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
+  }
+  fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *why = "tensor-core forward launch failed";
+  return e;
+}
+
+}  // namespace ra

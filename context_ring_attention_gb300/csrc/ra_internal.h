@@ -1,0 +1,116 @@
+// Internal declarations shared by the C ABI (ra_api.cu) and the kernels.
+//
+// Layout maps, the virtual-ring schedule and the causal tile rule live here so
+// that the host planner and every kernel use one definition of each.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ra.h"
+
+#ifdef __CUDACC__
+#define RA_HD __host__ __device__ __forceinline__
+#else
+#define RA_HD inline
+#endif
+
+namespace ra {
+
+constexpr int kTileRows = 128;  // query rows and key rows per tensor-core tile
+
+// Natural position of local row i of shard p (see include/ra.h).
+//   contiguous: p*S_N + i
+//   striped:    i*N + p            (Module 23, "The Causal Imbalance -- and the
+//                                   Striped Fix")
+//   zigzag:     chunk p then chunk 2N-1-p, chunks of c = S_N/2 rows
+RA_HD int64_t pos_of(int layout, int n_shards, int64_t s_n, int p, int64_t i) {
+  if (layout == RA_LAYOUT_STRIPED) return i * n_shards + p;
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const int64_t c = s_n >> 1;
+    return i < c ? p * c + i : (int64_t)(2 * n_shards - 1 - p) * c + (i - c);
+  }
+  return (int64_t)p * s_n + i;
+}
+
+// Largest local row j of shard r whose position is <= P, or -1.  Positions rise
+// with the local row in every layout, so the causal keys of a query at position P
+// within shard r are exactly rows 0..last_le(r, P).
+RA_HD int64_t last_le(int layout, int n_shards, int64_t s_n, int r, int64_t P) {
+  int64_t j;
+  if (layout == RA_LAYOUT_STRIPED) {
+    if (P < r) return -1;
+    j = (P - r) / n_shards;
+  } else if (layout == RA_LAYOUT_ZIGZAG) {
+    const int64_t c = s_n >> 1;
+    const int64_t lo = (int64_t)r * c;
+    const int64_t hi = (int64_t)(2 * n_shards - 1 - r) * c;
+    if (P < lo) return -1;
+    if (P < hi) j = (P - lo < c - 1) ? P - lo : c - 1;
+    else j = c + (P - hi);
+  } else {
+    j = P - (int64_t)r * s_n;
+    if (j < 0) return -1;
+  }
+  return j < s_n - 1 ? j : s_n - 1;
+}
+
+// Number of key tiles of shard r a query tile whose largest position is maxq
+// must visit: tiles past the last causal key are skipped (Module 23, "Exact by
+// Construction": blocks strictly in the future are skipped).
+RA_HD int visit_tiles(int layout, int n_shards, int64_t s_n, int causal, int r, int64_t maxq) {
+  const int nk = (int)((s_n + kTileRows - 1) / kTileRows);
+  if (!causal) return nk;
+  const int64_t j = last_le(layout, n_shards, s_n, r, maxq);
+  return j < 0 ? 0 : (int)(j / kTileRows) + 1;
+}
+
+// One unit of work for the tensor-core kernel: up to two 128-row query tiles
+// that share their key/value head and their tile schedule.
+struct alignas(16) WorkItem {
+  int32_t bh0;    // b*Hq + h of query tile 0
+  int32_t bh1;    // b*Hq + h of query tile 1, or -1 when the item has one tile
+  int32_t shard;  // p
+  int32_t row0;   // first local row (within shard p) of tile 0
+  int32_t row1;   // first local row of tile 1
+  int32_t maxq;   // largest natural position among the item's valid rows
+  int32_t cost;   // key tiles visited (longest-first ordering key)
+  int32_t pad;
+};
+
+struct FwdParams {
+  int32_t batch, heads_q, heads_kv, group, head_dim, n_shards, layout, causal;
+  int64_t seq, s_n;
+  int32_t n_items;
+  float scale;       // score scale
+  float scale_log2;  // scale * log2(e)
+  const WorkItem* items;
+  void* o;           // fused output, plan dtype
+  float* lse;        // fused LSE or nullptr
+  float* o_parts;    // partials mode outputs or nullptr
+  float* lse_parts;
+  uint32_t* status;  // device status word (bit set = a wait ran out of budget)
+};
+
+// Status bits written by kernels into the plan's status word.
+enum : uint32_t {
+  kStatusTimeoutProducer = 1u << 0,
+  kStatusTimeoutMma = 1u << 1,
+  kStatusTimeoutSoftmax = 1u << 2,
+  kStatusTimeoutTeardown = 1u << 3,
+};
+
+// Launchers (each returns cudaGetLastError() of its launch).
+cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, const void* v,
+                            int grid, cudaStream_t stream, const char** why);
+cudaError_t launch_fwd_f32(const FwdParams& prm, const float* q, const float* k, const float* v,
+                           cudaStream_t stream);
+cudaError_t launch_merge(int n_parts, int64_t rows, int d, const float* o_parts,
+                         const float* lse_parts, void* o, int o_dtype, float* lse,
+                         cudaStream_t stream);
+cudaError_t launch_layout_perm(int layout, int64_t seq, int n_shards, int inverse,
+                               int64_t rows_outer, int row_bytes, const void* src, void* dst,
+                               cudaStream_t stream);
+int fwd_bf16_smem_bytes();
+
+}  // namespace ra

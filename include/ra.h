@@ -1,0 +1,193 @@
+/*
+ * ra.h -- C ABI of the GB300 ring-attention forward library (libra.so).
+ *
+ * What the library computes (ring attention, forward):
+ *   Q, K and V are split along the sequence into N shards.  Shard p keeps its
+ *   query block; at ring step t = 0..N-1 it meets the K/V block of shard
+ *   r = (p - t) mod N ("device i -> i+1" rotation: "3.6 Distributed Training II",
+ *   section "Ring Attention"; the Q&A page "Explain ring attention ...", section
+ *   "The ring").  Each block is folded into a running max m, running sum l and
+ *   output accumulator o by the online-softmax update of "Module 23: Distributed
+ *   Training", section "The Math: One Block at a Time"; at the end O = o / l.
+ *   Causal attention skips blocks strictly in the future of a query tile and
+ *   masks the rest key by key on global positions (Module 23, "Exact by
+ *   Construction"); the diagonal is kept (key position <= query position).
+ *
+ *   One GPU runs all N shards: the ring rotation becomes the order in which
+ *   each query tile visits K/V tiles.  There are no inter-GPU transfers.
+ *
+ * Tensor conventions shared by every entry point:
+ *   - Q, O:   [B, Hq,  S, d] row-major, contiguous.
+ *   - K, V:   [B, Hkv, S, d] row-major, contiguous.
+ *   - LSE:    [B, Hq,  S] float32, natural-log log-sum-exp of the scaled,
+ *             masked scores of each row (the pages return O only; the LSE is
+ *             what lets partial results be merged).
+ *   - The S axis is in LAYOUT ORDER: shard p occupies rows [p*S/N, (p+1)*S/N),
+ *     and row p*S/N + i holds the token at natural position pos(p, i):
+ *       contiguous: p*S/N + i
+ *       striped:    i*N + p                 (Module 23, "The Causal Imbalance --
+ *                                            and the Striped Fix")
+ *       zigzag:     with c = S/(2N): i < c ? p*c + i : (2N-1-p)*c + (i - c)
+ *                   (reading of "the same idea, paired up block-by-block": chunk p
+ *                   paired with chunk 2N-1-p)
+ *     ra_layout_perm converts natural order <-> layout order.
+ *   - GQA: query head h reads key/value head h / (Hq/Hkv).
+ *   - Scores are s = scale * q.k with scale = 1/sqrt(d) unless given.
+ *
+ * Ownership: the caller owns every device buffer passed in.  A plan owns its
+ * host tables, its device work table and its device status word; ra_fwd,
+ * ra_merge_partials and ra_layout_perm allocate nothing and are asynchronous on
+ * the given stream (a cudaStream_t passed as void*; NULL = legacy default).
+ *
+ * Errors: every call returns an ra_status; on failure ra_last_error() returns a
+ * thread-local message.  Arguments are checked before anything is launched.
+ * Uneven shards are rejected, never padded (Module 23, "Common Pitfalls":
+ * reject uneven shards rather than silently bias the result).
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, uneven shards */
+  RA_ERR_UNSUPPORTED = 2,  /* valid problem outside what the kernels handle      */
+  RA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed               */
+  RA_ERR_TIMEOUT = 4,      /* a device-side wait exceeded its budget (~1 s)      */
+  RA_ERR_NO_DEVICE = 5     /* the plan has no device state (no GPU at plan time) */
+} ra_status;
+
+typedef enum {
+  RA_LAYOUT_CONTIGUOUS = 0,
+  RA_LAYOUT_STRIPED = 1,
+  RA_LAYOUT_ZIGZAG = 2
+} ra_layout;
+
+typedef enum {
+  RA_DTYPE_F32 = 0,   /* float32 Q/K/V/O; SIMT kernel, d <= 128              */
+  RA_DTYPE_BF16 = 1   /* bfloat16 Q/K/V/O; tensor-core kernel, d == 128      */
+} ra_dtype;
+
+/* One attention problem.  All sizes are element counts. */
+typedef struct {
+  int64_t batch;     /* B  >= 1                                            */
+  int64_t seq;       /* S  >= 1, multiple of n_shards (2*n_shards: zigzag) */
+  int32_t heads_q;   /* Hq >= 1, multiple of heads_kv                      */
+  int32_t heads_kv;  /* Hkv >= 1                                           */
+  int32_t head_dim;  /* d: 128 for BF16; 1..128 for F32                    */
+  int32_t n_shards;  /* N >= 1                                             */
+  int32_t layout;    /* ra_layout                                          */
+  int32_t causal;    /* 0 or 1                                             */
+  int32_t dtype;     /* ra_dtype                                           */
+  float scale;       /* score scale; 0 selects 1/sqrt(head_dim)            */
+} ra_problem;
+
+typedef struct ra_plan_s* ra_plan_t;
+
+/*
+ * ra_plan -- validate a problem and build its ring schedule.
+ * Builds, on the host, the list of query-tile work items in longest-first order
+ * with the per-shard tile classification (FULL / PARTIAL / SKIP, see
+ * ra_plan_tile_counts), and, when a CUDA device is current, uploads the work
+ * table and allocates the plan's device status word on it.  Without a device
+ * the plan is host-only: tile counts work, ra_fwd returns RA_ERR_NO_DEVICE.
+ * *out receives the plan; release it with ra_plan_destroy.
+ * Errors: RA_ERR_INVALID_ARG (null pointers, sizes < 1, S % N, zigzag S % 2N,
+ * Hq % Hkv, bad enum), RA_ERR_UNSUPPORTED (BF16 with d != 128, F32 with d > 128,
+ * more than 2^31 rows), RA_ERR_CUDA (device upload failed).
+ */
+ra_status ra_plan(const ra_problem* prob, ra_plan_t* out);
+
+/* Release a plan and its device memory.  NULL is accepted. */
+ra_status ra_plan_destroy(ra_plan_t plan);
+
+/*
+ * ra_plan_tile_counts -- per-shard causal tile classification of the schedule.
+ * For one (batch entry, query head), counts over all N ring steps the pairs
+ * (128-row query tile of shard p, 128-row key tile of the block met at step t)
+ * that are FULL (every (q,k) pair causal), PARTIAL (some) or SKIP (none),
+ * following Module 23's per-device causal work count ("The Causal Imbalance")
+ * at tile granularity.  The last tile of a shard may be shorter than 128.
+ * Non-causal problems count every tile FULL.  full, partial and skip are
+ * caller-owned host arrays of n_shards int64 each (any may be NULL).
+ */
+ra_status ra_plan_tile_counts(ra_plan_t plan, int64_t* full, int64_t* partial, int64_t* skip);
+
+/*
+ * ra_fwd -- ring-attention forward on the plan's problem.
+ * q, k, v: device pointers, layout order, dtype of the plan, 16-byte aligned.
+ * Fused mode (o_parts == lse_parts == NULL):
+ *   o   [B, Hq, S, d] in the plan's dtype (required);
+ *   lse [B, Hq, S] float32 (may be NULL).
+ * Partials mode (o_parts and lse_parts non-NULL, o == lse == NULL):
+ *   o_parts   [N, B, Hq, S, d] float32 and lse_parts [N, B, Hq, S] float32;
+ *   entry t of a row of shard p is attention of that row over the key block of
+ *   shard (p - t) mod N alone, normalised by its own sum; a block with no causal
+ *   key gives O_t = 0, LSE_t = -inf.  ra_merge_partials combines them.
+ * Asynchronous on stream; allocates nothing.  A device-side wait that runs out
+ * of budget makes the kernel return early and sets the plan's status word;
+ * ra_sync_status reports it.
+ * Errors: RA_ERR_INVALID_ARG (null/misaligned pointers, mixed modes),
+ * RA_ERR_NO_DEVICE, RA_ERR_CUDA (launch failure).
+ */
+ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v,
+                 void* o, float* lse, float* o_parts, float* lse_parts, void* stream);
+
+/*
+ * ra_merge_partials -- exact combination of partial attention results.
+ * For each of `rows` rows: LSE = ln sum_t e^(LSE_t), O = sum_t e^(LSE_t - LSE) O_t
+ * (order independence of the online-softmax fold, Module 23, "The Math: One
+ * Block at a Time").  Parts with LSE_t = -inf are ignored; a row whose parts are
+ * all -inf gets O = 0 and LSE = -inf.
+ * o_parts [n_parts, rows, d] float32, lse_parts [n_parts, rows] float32, o [rows, d]
+ * in o_dtype (F32 or BF16, round-to-nearest-even), lse [rows] float32 or NULL.
+ * Device pointers, 16-byte aligned.  Asynchronous on stream; allocates nothing.
+ * Errors: RA_ERR_INVALID_ARG (sizes < 1, d > 1024, null/misaligned pointers),
+ * RA_ERR_CUDA.
+ */
+ra_status ra_merge_partials(int32_t n_parts, int64_t rows, int32_t d,
+                            const float* o_parts, const float* lse_parts,
+                            void* o, int32_t o_dtype, float* lse, void* stream);
+
+/*
+ * ra_layout_perm -- move whole rows between natural order and layout order.
+ * src and dst are [rows_outer, seq, row_bytes] (e.g. Q as [B*Hq, S, d*2] bytes).
+ * inverse == 0: dst[o, j] = src[o, pos(j)]   (natural -> layout order)
+ * inverse != 0: dst[o, pos(j)] = src[o, j]   (layout -> natural order)
+ * with pos the layout map above.  row_bytes must be a multiple of 4; pointers
+ * 16-byte aligned; src and dst must not overlap.  Asynchronous; allocates nothing.
+ * Errors: RA_ERR_INVALID_ARG (uneven shards, bad sizes, overlap, alignment),
+ * RA_ERR_CUDA.
+ */
+ra_status ra_layout_perm(int32_t layout, int64_t seq, int32_t n_shards, int32_t inverse,
+                         int64_t rows_outer, int32_t row_bytes,
+                         const void* src, void* dst, void* stream);
+
+/*
+ * ra_layout_index -- host helper: pos_out[j] = natural position of layout row j,
+ * for j in [0, seq).  pos_out is a caller-owned host array of seq int64.
+ * Errors: RA_ERR_INVALID_ARG (uneven shards, null pointer, bad layout).
+ */
+ra_status ra_layout_index(int32_t layout, int64_t seq, int32_t n_shards, int64_t* pos_out);
+
+/*
+ * ra_sync_status -- synchronize `stream`, then read and clear the plan's device
+ * status word.  Returns RA_ERR_TIMEOUT if a kernel launched with this plan gave
+ * up on a device-side wait since the last call, RA_ERR_CUDA on a CUDA error,
+ * RA_OK otherwise.
+ */
+ra_status ra_sync_status(ra_plan_t plan, void* stream);
+
+/* Thread-local message describing the last failure on this thread ("" if none). */
+const char* ra_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

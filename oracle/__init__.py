@@ -29,6 +29,7 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
                             (one key, identical keys, causal row 0); row sums of 1;
                             GQA head mapping against per-head single-head calls.
 ``full_attention_rows``     equals ``full_attention`` row by row.
+``attention_rows``          equals ``full_attention`` row by row (causal, by position).
 ``ring_sim``                the Q&A page's 4-device toy (seed 1) equals ordinary attention;
                             Module 23's (2,4,96,32) example, full and causal, within the
                             page's 1e-5; layout invariance after un-permuting.
@@ -43,7 +44,7 @@ No function here is "parity unpinned".
 """
 
 from .layouts import CONTIGUOUS, STRIPED, ZIGZAG, LAYOUTS, layout_positions, causal_pair_counts
-from .attention import full_attention, full_attention_rows
+from .attention import attention_rows, full_attention, full_attention_rows
 from .ring import ring_sim, ring_partials
 from .merge import merge_partials
 from .tiles import tile_counts, tile_classes_bruteforce
@@ -51,7 +52,7 @@ from .tiles import tile_counts, tile_classes_bruteforce
 __all__ = [
     "CONTIGUOUS", "STRIPED", "ZIGZAG", "LAYOUTS",
     "layout_positions", "causal_pair_counts",
-    "full_attention", "full_attention_rows",
+    "full_attention", "full_attention_rows", "attention_rows",
     "ring_sim", "ring_partials", "merge_partials",
     "tile_counts", "tile_classes_bruteforce",
 ]

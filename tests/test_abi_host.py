@@ -1,0 +1,124 @@
+"""Host-side tests of libra.so: exports, argument checks, planner, layout maps.
+
+No GPU is needed: the planner's tile counts and the layout maps are pure host
+code, checked bit for bit against the oracle.  Nothing here launches a kernel.
+"""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.conftest import ROOT
+
+ra = pytest.importorskip("context_ring_attention_gb300")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from context_ring_attention_gb300 import build
+    if not os.path.exists(ra.library_path()):
+        build.build()
+    return ra.load_library()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "ra.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_symbols()
+    assert set(names) == set(ra.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_device_plan_refuses_fwd(lib):
+    pytest.importorskip("torch")
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    plan = ra.ra_plan(1, 256, 2, 2, 128, 2, "contiguous", True, "bf16")
+    buf = ctypes.create_string_buffer(4096 + 16)
+    addr = (ctypes.addressof(buf) + 15) & ~15
+    st = lib.ra_fwd(plan.handle, addr, addr, addr, addr, None, None, None, None)
+    assert st == 5   # RA_ERR_NO_DEVICE
+    assert "without a CUDA device" in ra.ra_last_error()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(seq=100, n_shards=8), 1),                                  # uneven shards
+    (dict(seq=20, n_shards=4, layout="zigzag"), 1),                 # zigzag needs 2N | S
+    (dict(heads_q=6, heads_kv=4), 1),                               # Hq % Hkv
+    (dict(head_dim=64), 2),                                         # bf16 needs d == 128
+    (dict(dtype="f32", head_dim=256), 2),                           # f32 d <= 128
+    (dict(batch=0), 1),
+    (dict(scale=-1.0), 1),
+])
+def test_plan_rejects(lib, kw, status):
+    args = dict(batch=1, seq=1024, heads_q=4, heads_kv=2, head_dim=128, n_shards=8, layout="contiguous",
+                causal=True, dtype="bf16", scale=0.0)
+    args.update(kw)
+    with pytest.raises(ra.RaError) as ei:
+        ra.ra_plan(**args)
+    assert ei.value.status == status
+
+
+def test_null_arguments(lib):
+    assert lib.ra_plan(None, None) == 1
+    assert lib.ra_plan_tile_counts(None, None, None, None) == 1
+    assert lib.ra_merge_partials(0, 1, 1, None, None, None, 0, None, None) == 1
+    assert lib.ra_layout_perm(0, 8, 2, 0, 1, 4, None, None, None) == 1
+    assert lib.ra_layout_index(0, 8, 3, None) == 1
+    assert lib.ra_plan_destroy(None) == 0
+
+
+def test_layout_perm_rejects_overlap_and_alignment(lib):
+    buf = ctypes.create_string_buffer(8192 + 32)
+    a = (ctypes.addressof(buf) + 15) & ~15
+    assert lib.ra_layout_perm(0, 16, 2, 0, 1, 4, a, a + 16, None) == 1      # overlap
+    assert lib.ra_layout_perm(0, 16, 2, 0, 1, 4, a + 4, a + 4096, None) == 1  # misaligned
+    assert lib.ra_layout_perm(0, 16, 2, 0, 1, 6, a, a + 4096, None) == 1     # row_bytes % 4
+
+
+@pytest.mark.parametrize("layout", oracle.LAYOUTS)
+@pytest.mark.parametrize("seq,n", [(12, 4), (96, 8), (4096, 32), (32768, 8), (1000, 10)])
+def test_layout_index_matches_oracle(lib, layout, seq, n):
+    if layout == "zigzag" and seq % (2 * n):
+        pytest.skip("zigzag needs 2N | S")
+    assert ra.ra_layout_index(layout, seq, n).tolist() == oracle.layout_positions(layout, seq, n).tolist()
+
+
+CASES = [
+    ("contiguous", 32768, 8), ("zigzag", 32768, 8), ("striped", 131072, 32), ("zigzag", 1048576, 8),
+    ("contiguous", 1000, 4), ("striped", 1000, 4), ("zigzag", 1000, 4), ("striped", 96 * 8, 8),
+    ("zigzag", 4 * 300, 2), ("contiguous", 12, 4), ("striped", 640, 5),
+]
+
+
+@pytest.mark.parametrize("layout,seq,n", CASES)
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_counts_match_oracle(lib, layout, seq, n, causal):
+    plan = ra.ra_plan(1, seq, 4, 2, 128, n, layout, causal, "bf16")
+    got = ra.ra_plan_tile_counts(plan)
+    want = oracle.tile_counts(layout, seq, n, causal=causal, tile=128)
+    for g, w in zip(got, want):
+        assert g.tolist() == w.tolist()
+
+
+def test_tile_counts_seq32k_report():
+    """The per-shard FULL/PARTIAL/SKIP table for 32768 tokens, 8 shards (reported by bench)."""
+    for layout in ("contiguous", "zigzag"):
+        plan = ra.ra_plan(1, 32768, 32, 8, 128, 8, layout, True, "bf16")
+        full, part, skip = ra.ra_plan_tile_counts(plan)
+        assert (full + part + skip).tolist() == [32 * 32 * 8] * 8
+        if layout == "zigzag":
+            assert len(set((full + part).tolist())) == 1          # exactly balanced
+        else:
+            assert (full + part).tolist() == sorted((full + part).tolist())

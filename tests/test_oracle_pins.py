@@ -313,3 +313,19 @@ def test_tile_counts_closed_forms_striped_131k():
 def test_oracle_exports():
     for name in oracle.__all__:
         assert hasattr(oracle, name)
+
+
+def test_attention_rows_equals_full():
+    q = _rand((1, 2, 50, 8), 50)
+    k, v = _rand((1, 1, 50, 8), 51), _rand((1, 1, 50, 8), 52)
+    pos = layout_positions(STRIPED, 50, 5)
+    o, lse = full_attention(q, k, v, causal=True)            # natural order
+    rows = np.array([0, 3, 17, 49, 25])
+    o2, l2 = oracle.attention_rows(q[0, 1, rows], k[0, 0], v[0, 0], q_positions=rows, causal=True, chunk=2)
+    np.testing.assert_allclose(o2, o[0, 1, rows], atol=1e-14)
+    np.testing.assert_allclose(l2, lse[0, 1, rows], atol=1e-14)
+    # keys handed over in layout order with their positions give the same rows
+    o3, l3 = oracle.attention_rows(q[0, 1, rows], k[0, 0, pos], v[0, 0, pos], q_positions=rows,
+                                   k_positions=pos, causal=True)
+    np.testing.assert_allclose(o3, o2, atol=1e-14)
+    np.testing.assert_allclose(l3, l2, atol=1e-14)
