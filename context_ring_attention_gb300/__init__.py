@@ -209,15 +209,13 @@ def ra_merge_partials(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stre
 def ra_layout_perm(x, layout, n_shards, inverse=False, seq_dim=None, out=None, stream=None):
     """Natural -> layout order (inverse=False) or back, along ``seq_dim``.
 
-    ``seq_dim`` defaults to -2 for tensors of 3+ dims ([..., S, d]) and -1 otherwise
-    ([..., S], e.g. an LSE).  Everything after the sequence axis moves as one row.
+    ``seq_dim`` defaults to 2, the sequence axis of the library's [B, H, S, d] and
+    [B, H, S] tensors.  Everything after the sequence axis moves as one row.
     """
     import torch
     if not x.is_contiguous():
         raise ValueError("x must be contiguous")
-    if seq_dim is None:
-        seq_dim = -2 if x.dim() >= 3 else -1
-    seq_dim = seq_dim % x.dim()
+    seq_dim = (2 if seq_dim is None else seq_dim) % x.dim()
     seq = x.shape[seq_dim]
     outer = int(np.prod(x.shape[:seq_dim], dtype=np.int64)) if seq_dim else 1
     row_bytes = int(np.prod(x.shape[seq_dim + 1:], dtype=np.int64)) * x.element_size()

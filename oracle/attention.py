@@ -110,24 +110,32 @@ def attention_rows(q_rows, k_head, v_head, q_positions=None, k_positions=None, c
 
     q_rows: [n, d]; k_head, v_head: [S, d]; positions are natural token positions
     (needed when causal).  The plain definition again, one row block at a time so
-    that million-key heads fit in memory.  Returns O [n, d], LSE [n] in float64.
+    that million-key heads fit in memory.  When the keys are given in natural
+    order (k_positions None) a causal row block only reads keys up to its largest
+    position: later keys are masked and carry no weight.
+    Returns O [n, d], LSE [n] in float64.
     """
     q_rows = np.asarray(q_rows, dtype=np.float64)
-    k_head = np.asarray(k_head, dtype=np.float64)
-    v_head = np.asarray(v_head, dtype=np.float64)
     n, d = q_rows.shape
     sc = _scale(d, scale)
     out = np.zeros((n, d))
     lse = np.full(n, -np.inf)
+    natural_keys = k_positions is None
+    order = np.arange(n)
     if causal:
         qp = np.asarray(q_positions, np.int64)
-        kp = np.arange(k_head.shape[0], dtype=np.int64) if k_positions is None \
-            else np.asarray(k_positions, np.int64)
-    for r0 in range(0, n, chunk):
-        r1 = min(n, r0 + chunk)
-        s = (q_rows[r0:r1] @ k_head.T) * sc
+        kp = np.arange(k_head.shape[0], dtype=np.int64) if natural_keys else np.asarray(k_positions, np.int64)
+        order = np.argsort(qp, kind="stable")
+    for c0 in range(0, n, chunk):
+        rows = order[c0:c0 + chunk]
+        limit = k_head.shape[0]
+        if causal and natural_keys:
+            limit = int(qp[rows].max()) + 1
+        kh = np.asarray(k_head[:limit], dtype=np.float64)
+        vh = np.asarray(v_head[:limit], dtype=np.float64)
+        s = (q_rows[rows] @ kh.T) * sc
         if causal:
-            s = np.where(kp[None, :] <= qp[r0:r1, None], s, -np.inf)
+            s = np.where(kp[None, :limit] <= qp[rows, None], s, -np.inf)
         row_max = s.max(axis=1)
         live = np.isfinite(row_max)
         shift = np.where(live, row_max, 0.0)
@@ -135,6 +143,6 @@ def attention_rows(q_rows, k_head, v_head, q_positions=None, k_positions=None, c
         z = e.sum(axis=1)
         with np.errstate(divide="ignore", invalid="ignore"):
             probs = np.where(live[:, None], e / z[:, None], 0.0)
-            lse[r0:r1] = np.where(live, shift + np.log(z), -np.inf)
-        out[r0:r1] = probs @ v_head
+            lse[rows] = np.where(live, shift + np.log(z), -np.inf)
+        out[rows] = probs @ vh
     return out, lse

@@ -1,0 +1,60 @@
+"""Run the row oracle over many query rows on all host cores.
+
+The rows are independent, so they are split over a process pool (``spawn``: a
+pool forked after CUDA initialisation can hang).  Each worker memory-maps the
+key/value head from a temporary .npy file instead of receiving a copy.
+"""
+
+import multiprocessing as mp
+import os
+import shutil
+import tempfile
+
+import numpy as np
+
+_K = _V = None
+
+
+def _init(kpath, vpath):
+    global _K, _V
+    _K = np.load(kpath, mmap_mode="r")
+    _V = np.load(vpath, mmap_mode="r")
+
+
+def _work(args):
+    import oracle
+    q_rows, q_pos, causal, scale = args
+    return oracle.attention_rows(q_rows, _K, _V, q_positions=q_pos, causal=causal, scale=scale)
+
+
+def attention_rows_parallel(q_rows, q_pos, k_head, v_head, causal, scale=None, workers=None, chunk=64):
+    """oracle.attention_rows over natural-order keys, rows spread over processes."""
+    q_rows = np.asarray(q_rows, np.float64)
+    q_pos = np.asarray(q_pos, np.int64)
+    n = q_rows.shape[0]
+    workers = workers or min(16, os.cpu_count() or 1)
+    tmp = tempfile.mkdtemp(prefix="ra_oracle_")
+    try:
+        kpath, vpath = os.path.join(tmp, "k.npy"), os.path.join(tmp, "v.npy")
+        np.save(kpath, np.asarray(k_head, np.float32))
+        np.save(vpath, np.asarray(v_head, np.float32))
+        order = np.argsort(q_pos, kind="stable")
+        # interleave sorted rows so every task has a similar key range
+        tasks, idx = [], []
+        n_tasks = max(1, min(workers * 4, (n + chunk - 1) // chunk))
+        for t in range(n_tasks):
+            sel = order[t::n_tasks]
+            if sel.size:
+                tasks.append((q_rows[sel], q_pos[sel], causal, scale))
+                idx.append(sel)
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(workers, initializer=_init, initargs=(kpath, vpath)) as pool:
+            res = pool.map(_work, tasks)
+        out = np.zeros((n, q_rows.shape[1]))
+        lse = np.full(n, -np.inf)
+        for sel, (o, l) in zip(idx, res):
+            out[sel] = o
+            lse[sel] = l
+        return out, lse
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)

@@ -41,7 +41,7 @@ def test_layout_perm_bitexact(layout, seq, n):
     assert torch.equal(ra.ra_layout_perm(ly, layout, n, inverse=True), lse)
     # fp32 rows of 12 bytes (3 floats) take the 4-byte path
     z = torch.randn((5, seq, 3), generator=g, device="cuda")
-    assert torch.equal(ra.ra_layout_perm(z, layout, n), z.index_select(1, pos_t))
+    assert torch.equal(ra.ra_layout_perm(z, layout, n, seq_dim=1), z.index_select(1, pos_t))
 
 
 # ------------------------------------------------------------------ merge --
