@@ -19,7 +19,7 @@ import numpy as np
 __all__ = [
     "RaError", "Plan", "LAYOUTS",
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
-    "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error",
+    "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -28,7 +28,7 @@ DTYPES = {"f32": 0, "bf16": 1}
 _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
            4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
-            "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error")
+            "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -72,6 +72,7 @@ def load_library():
         "ra_layout_index": ([I32, I64, I32, VP], I32),
         "ra_sync_status": ([P, VP], I32),
         "ra_last_error": ([], ctypes.c_char_p),
+        "ra_fwd_static": ([ctypes.POINTER(_Problem), VP, VP, VP, VP, VP, VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -236,3 +237,23 @@ def ra_layout_index(layout, seq, n_shards):
 def ra_sync_status(plan, stream=None):
     """Synchronize the stream and raise RaError if a device wait of this plan timed out."""
     _check(load_library().ra_sync_status(plan.handle, _stream(stream)))
+
+
+def ra_fwd_static(batch, seq, heads_q, heads_kv, n_shards, layout, causal, q, k, v, o=None, lse=None,
+                  scale=0.0, stream=None):
+    """Fused bf16 forward without a plan and without allocating device memory.
+
+    For callers that must not allocate device memory at run time (the library's
+    static scratch array holds the work list).  Returns (O, LSE); pass ``o`` and
+    ``lse`` to avoid the two torch allocations this wrapper otherwise makes.
+    """
+    import torch
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((batch, heads_q, seq), dtype=torch.float32, device=q.device)
+    prob = _Problem(int(batch), int(seq), int(heads_q), int(heads_kv), 128, int(n_shards), _layout(layout),
+                    int(bool(causal)), 1, float(scale or 0.0))
+    _check(load_library().ra_fwd_static(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                        _stream(stream)))
+    return o, lse

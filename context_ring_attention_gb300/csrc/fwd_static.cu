@@ -1,0 +1,182 @@
+// ra_fwd_static: the bf16 ring forward for callers that cannot allocate memory.
+//
+// Some callers cannot call cudaMalloc at run time -- code that runs under a
+// memory pool or allocator it must not bypass, or that has to fix its whole
+// device footprint at load time -- and so cannot create a plan (ra_plan
+// allocates the work table and status word).  This entry point needs no plan:
+// the work table and the status word live in one file-scope device array of
+// fixed size, which every GPU that loads this library holds until the process
+// exits.  Nothing here calls cudaMalloc, cudaFree or any allocating routine;
+// the host-side work list is built in a static host buffer.
+//
+// The device array is shared by every call: calls whose kernels overlap on the
+// GPU (other streams, other host threads) race on it.  Calls from several host
+// threads are serialised on the host while the work list is built and copied.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "ra_internal.h"
+
+namespace {
+
+constexpr int kMaxItems = 131072;           // work items: e.g. 1M tokens x 32 query heads
+constexpr size_t kStatusBytes = 256;        // status word at the start of the array
+constexpr size_t kScratchBytes = kStatusBytes + (size_t)kMaxItems * sizeof(ra::WorkItem);  // 4 MiB + 256 B
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+struct Keyed {
+  ra::WorkItem w;
+  int64_t order;
+};
+Keyed g_host_items[kMaxItems];  // host staging for the work list
+std::mutex g_mutex;
+void* g_dev_addr[kMaxDevices] = {};  // device address of g_scratch, per device
+int g_dev_sms[kMaxDevices] = {};
+
+ra_status fail(ra_status s, const char* msg) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "ra_fwd_static: %s", msg);
+  ra::set_last_error(buf);
+  return s;
+}
+
+ra_status check_problem(const ra_problem* p) {
+  if (p == nullptr) return fail(RA_ERR_INVALID_ARG, "null problem");
+  if (p->batch < 1 || p->heads_q < 1 || p->heads_kv < 1 || p->n_shards < 1 || p->seq < 1)
+    return fail(RA_ERR_INVALID_ARG, "sizes must be >= 1");
+  if (p->layout < RA_LAYOUT_CONTIGUOUS || p->layout > RA_LAYOUT_ZIGZAG) return fail(RA_ERR_INVALID_ARG, "bad layout");
+  if (p->seq % p->n_shards) return fail(RA_ERR_INVALID_ARG, "seq is not a multiple of n_shards");
+  if (p->layout == RA_LAYOUT_ZIGZAG && p->seq % (2 * (int64_t)p->n_shards))
+    return fail(RA_ERR_INVALID_ARG, "zigzag needs seq to be a multiple of 2*n_shards");
+  if (p->heads_q % p->heads_kv) return fail(RA_ERR_INVALID_ARG, "heads_q is not a multiple of heads_kv");
+  if (p->causal != 0 && p->causal != 1) return fail(RA_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!(p->scale >= 0.f) || std::isinf(p->scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  if (p->dtype != RA_DTYPE_BF16 || p->head_dim != 128)
+    return fail(RA_ERR_UNSUPPORTED, "only bf16 with head_dim 128 is supported");
+  if (p->seq > INT32_MAX || p->batch > INT32_MAX / p->heads_q || p->batch * (int64_t)p->heads_q * p->seq > INT32_MAX)
+    return fail(RA_ERR_UNSUPPORTED, "more than 2^31-1 rows");
+  return RA_OK;
+}
+
+// The planner's work list (same items, same longest-first order), written into
+// the static host buffer.  Returns the item count, or -1 when it would not fit.
+int64_t build_items(const ra_problem& pb) {
+  const int N = pb.n_shards;
+  const int64_t s_n = pb.seq / N;
+  const int n_qt = (int)((s_n + ra::kTileRows - 1) / ra::kTileRows);
+  const bool head_pairs = ((pb.heads_q / pb.heads_kv) % 2) == 0;
+  const int64_t per_shard = head_pairs ? (int64_t)n_qt * pb.batch * (pb.heads_q / 2)
+                                       : (int64_t)((n_qt + 1) / 2) * pb.batch * pb.heads_q;
+  if (per_shard * N > kMaxItems) return -1;
+  int64_t n = 0;
+  for (int p = 0; p < N; ++p)
+    for (int qt = 0; qt < n_qt; qt += head_pairs ? 1 : 2)
+      for (int64_t b = 0; b < pb.batch; ++b)
+        for (int h = 0; h < pb.heads_q; h += head_pairs ? 2 : 1) {
+          ra::WorkItem w{};
+          w.bh0 = (int32_t)(b * pb.heads_q + h);
+          w.shard = p;
+          w.row0 = qt * ra::kTileRows;
+          if (head_pairs) {
+            w.bh1 = w.bh0 + 1;
+            w.row1 = w.row0;
+          } else if (qt + 1 < n_qt) {
+            w.bh1 = w.bh0;
+            w.row1 = w.row0 + ra::kTileRows;
+          } else {
+            w.bh1 = -1;
+            w.row1 = w.row0;
+          }
+          const int64_t top = std::min<int64_t>((w.bh1 >= 0 ? w.row1 : w.row0) + ra::kTileRows, s_n) - 1;
+          w.maxq = (int32_t)ra::pos_of(pb.layout, N, s_n, p, top);
+          int cost = 0;
+          for (int t = 0; t < N; ++t) cost += ra::visit_tiles(pb.layout, N, s_n, pb.causal, (p - t + N) % N, w.maxq);
+          w.cost = cost;
+          g_host_items[n] = {w, n};
+          ++n;
+        }
+  std::sort(g_host_items, g_host_items + n, [](const Keyed& a, const Keyed& b) {
+    return a.w.cost != b.w.cost ? a.w.cost > b.w.cost : a.order < b.order;
+  });
+  return n;
+}
+
+}  // namespace
+
+extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const void* k, const void* v,
+                                   void* o, float* lse, void* stream) {
+  ra_status s = check_problem(prob);
+  if (s != RA_OK) return s;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return fail(RA_ERR_INVALID_ARG, "null pointer");
+  const void* ptrs[] = {q, k, v, o, lse};
+  for (const void* p : ptrs)
+    if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u)) return fail(RA_ERR_INVALID_ARG, "pointer not 16-byte aligned");
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  const int64_t n_items = build_items(*prob);
+  if (n_items < 0) return fail(RA_ERR_UNSUPPORTED, "work list exceeds the static maximum of 131072 items");
+
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_NO_DEVICE, "no CUDA device");
+  }
+  if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device ordinal above 63");
+  if (g_dev_addr[dev] == nullptr) {
+    // First call on this device (which is current): look up the array's device address.
+    void* addr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&addr, g_scratch);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, cudaGetErrorString(e));
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, cudaGetErrorString(e));
+    g_dev_sms[dev] = sms;
+    g_dev_addr[dev] = addr;
+  }
+  unsigned char* base = static_cast<unsigned char*>(g_dev_addr[dev]);
+  ra::WorkItem* d_items = reinterpret_cast<ra::WorkItem*>(base + kStatusBytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // The sorted items without their sort keys, contiguous for the copy.
+  static ra::WorkItem packed[kMaxItems];
+  for (int64_t i = 0; i < n_items; ++i) packed[i] = g_host_items[i].w;
+  // Pageable-source async copies return once the source has been staged, so the
+  // static host buffer may be reused by the next call.
+  cudaError_t e = cudaMemcpyAsync(d_items, packed, (size_t)n_items * sizeof(ra::WorkItem), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, sizeof(uint32_t), st);  // status word starts clear
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, cudaGetErrorString(e));
+
+  ra::FwdParams prm{};
+  prm.batch = (int32_t)prob->batch;
+  prm.heads_q = prob->heads_q;
+  prm.heads_kv = prob->heads_kv;
+  prm.group = prob->heads_q / prob->heads_kv;
+  prm.head_dim = prob->head_dim;
+  prm.n_shards = prob->n_shards;
+  prm.layout = prob->layout;
+  prm.causal = prob->causal;
+  prm.seq = prob->seq;
+  prm.s_n = prob->seq / prob->n_shards;
+  prm.n_items = (int32_t)n_items;
+  prm.scale = prob->scale > 0.f ? prob->scale : 1.0f / std::sqrt(128.0f);
+  prm.scale_log2 = prm.scale * 1.4426950408889634f;
+  prm.items = d_items;
+  prm.o = o;
+  prm.lse = lse;
+  prm.o_parts = nullptr;
+  prm.lse_parts = nullptr;
+  prm.status = reinterpret_cast<uint32_t*>(base);
+  if (n_items == 0) return RA_OK;
+  const int grid = (int)std::min<int64_t>(n_items, g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 148);
+  const char* why = "";
+  e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, why);
+  ra::set_last_error("");
+  return RA_OK;
+}

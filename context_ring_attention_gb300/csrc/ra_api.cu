@@ -200,6 +200,8 @@ ra_status upload(ra_plan_s* pl) {
 
 }  // namespace
 
+void ra::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 extern "C" {
 
 ra_status ra_plan(const ra_problem* prob, ra_plan_t* out) {

@@ -113,4 +113,7 @@ cudaError_t launch_layout_perm(int layout, int64_t seq, int n_shards, int invers
                                cudaStream_t stream);
 int fwd_bf16_smem_bytes();
 
+// Sets the thread-local message returned by ra_last_error().
+void set_last_error(const char* msg);
+
 }  // namespace ra

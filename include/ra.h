@@ -183,6 +183,36 @@ ra_status ra_layout_index(int32_t layout, int64_t seq, int32_t n_shards, int64_t
  */
 ra_status ra_sync_status(ra_plan_t plan, void* stream);
 
+/*
+ * ra_fwd_static -- the bf16 fused forward for callers that cannot allocate.
+ * The pages have no counterpart to this entry point; it exists for callers that
+ * must not allocate device memory at run time (code running under an allocator
+ * or memory pool it may not bypass, or with a device footprint fixed at load
+ * time) and therefore cannot create a plan, since ra_plan allocates the work
+ * table and status word.  It computes exactly what ra_fwd computes in fused mode
+ * for a bf16, head_dim 128 problem, without a plan and without allocating:
+ * no cudaMalloc, cudaFree or other allocating routine is called.
+ *   - Scratch: the work table and status word live in one file-scope device
+ *     array of 4 MiB + 256 B, held on every GPU that loads the library until the
+ *     process exits.  Problems needing more than 131072 work items (one item per
+ *     pair of 128-row query tiles; e.g. 1M tokens x 32 query heads is exactly
+ *     131072) are rejected with RA_ERR_UNSUPPORTED.
+ *   - Set-up: the first call on a device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - Sharing: every call reuses the array; the status word is cleared at the
+ *     start of each call.  Calls whose kernels overlap on the GPU race on the
+ *     array and must not be issued; calls from several host threads are
+ *     serialised on the host.  Device-side wait timeouts are recorded in the
+ *     array's status word but not reported (use a plan and ra_sync_status for that).
+ * prob: the problem (dtype RA_DTYPE_BF16, head_dim 128).  q, k, v, o, lse: as for
+ * ra_fwd in fused mode (lse may be NULL), device pointers, 16-byte aligned.
+ * Asynchronous on stream.
+ * Errors: RA_ERR_INVALID_ARG, RA_ERR_UNSUPPORTED (dtype, head_dim, size),
+ * RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ */
+ra_status ra_fwd_static(const ra_problem* prob, const void* q, const void* k, const void* v,
+                        void* o, float* lse, void* stream);
+
 /* Thread-local message describing the last failure on this thread ("" if none). */
 const char* ra_last_error(void);
 
