@@ -13,9 +13,10 @@
 //              ring order into a 3-slot shared-memory ring (128B swizzle).
 //   warp 1     tcgen05 issuer: S = Q K^T into TMEM, O += P V into TMEM.
 //   warps 4-7  softmax for query tile 0, warps 8-11 for query tile 1: one thread
-//              per row reads S from TMEM, updates m and l, writes P (bf16) to
-//              shared memory, rescales O in TMEM when m moves, and writes O / l
-//              and the LSE at the end of a segment.
+//              per row reads its 128 scores from TMEM in one round trip, updates
+//              m and l, writes P (bf16) to shared memory, rescales O in TMEM when
+//              m moves, and writes O / l and the LSE at the end of a segment.
+//   Warpgroup 0 (warps 0-3) hands registers to the softmax warpgroups (setmaxnreg).
 // Two query tiles per CTA let one tile's softmax overlap the other tile's MMAs.
 // TMEM: S0 cols 0-127, S1 128-255, O0 256-383, O1 384-511 (all 512 columns).
 //
@@ -33,7 +34,14 @@
 namespace ra {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 384;  // 3 warpgroups: {producer, MMA, 2 idle}, softmax 0, softmax 1
+// Register split (per thread): launched at kRegsLaunch; warpgroup 0 gives registers
+// back so the two softmax warpgroups can hold a whole 128-score row.
+// 128 * kRegsOther + 256 * kRegsSoftmax must not exceed 384 * kRegsLaunch.
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsOther = 120;
+constexpr uint32_t kRegsSoftmax = 192;
+static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
 constexpr uint32_t kHalfBytes = 128 * 64 * 2;   // 128 rows x one 128-byte swizzle column
 constexpr int kStages = 3;
@@ -76,7 +84,7 @@ struct Ctl {
 };
 
 // Bounded wait for phase `parity` of a barrier; false on abort or expiry.
-__device__ __noinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t parity, uint32_t who) {
+__device__ __forceinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t parity, uint32_t who) {
   if (ptx::mbar_test(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -93,7 +101,7 @@ __device__ __noinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t parit
 }
 
 // Teardown wait: ignores the abort flag, still bounded.
-__device__ __noinline__ void drain_bar(const Ctl& c, uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_bar(const Ctl& c, uint32_t bar, uint32_t parity) {
   const uint64_t t0 = ptx::global_timer_ns();
   while (!ptx::mbar_test(bar, parity)) {
     if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
@@ -322,7 +330,7 @@ __device__ __forceinline__ void store_segment(const FwdParams& P, uint32_t tO, f
 
 __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32_t tmem, int g,
                             int wq, int lane) {
-  const int row = wq * 32 + lane;
+  const int row = wq * 32 + lane;  // TMEM lane = query row of the tile
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + col_s(g);
   const uint32_t tO = tmem + lane_off + col_o(g);
@@ -376,22 +384,24 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
         if (!__all_sync(0xffffffffu, ok)) return;
         ptx::tc_fence_after();
 
-        // Pass 1: row max of the (masked) raw scores.
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          __syncwarp();
-          ptx::tmem_ld32(tS + cc * 32, v);
-          if (limit >= (cc + 1) * 32) {
+        // The whole 128-column score row in registers (one TMEM round trip).
+        uint32_t raw[128];
+        ptx::tmem_ld128(tS, raw);
+        float* s = reinterpret_cast<float*>(raw);
+        if (limit < kTileRows) {  // causal diagonal / ragged tail: masked keys score -inf
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (cc * 32 + e < limit) mx = fmaxf(mx, __uint_as_float(v[e]));
-          }
+          for (int e = 0; e < 128; ++e) s[e] = (e < limit) ? s[e] : -INFINITY;
         }
+        // Row max with independent partial maxima (no long dependency chain).
+        float mx8[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx8[a] = ptx::max3(s[a], s[a + 8], s[a + 16]);
+#pragma unroll
+        for (int e = 24; e + 16 <= 128; e += 16)
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx8[a] = ptx::max3(mx8[a], s[e + a], s[e + 8 + a]);
+        const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
+                               fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float mt = mx * sl2;  // in log2 units; -inf stays -inf
         float m_new = m;
         bool resc = false;
@@ -402,9 +412,40 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
           m_new = mt;
           resc = true;
         }
+        const float alpha = resc ? ptx::ex2_approx(m - m_new) : 1.0f;
+        m = m_new;
+        const float mref = (m == -INFINITY) ? 0.f : m;
+
+        // p = 2^(s*scale*log2e - m) (masked -inf -> 0), row sum, P to shared memory as bf16.
+        const float2 sc2 = make_float2(sl2, sl2);
+        const float2 neg = make_float2(-mref, -mref);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k0 = cc * 32 + 2 * e;
+            float2 x = ptx::fma2(make_float2(s[k0], s[k0 + 1]), sc2, neg);
+            x.x = ptx::ex2_approx(x.x);
+            x.y = ptx::ex2_approx(x.y);
+            acc[e & 3] = ptx::add2(acc[e & 3], x);
+            w[e] = ptx::pack_bf16x2(x.x, x.y);
+          }
+          const uint32_t line = prow + (uint32_t)(cc >> 1) * kHalfBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t chunk = (uint32_t)((cc & 1) * 4 + j);
+            ptx::st_shared_v4(line + ((chunk ^ rsw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
+        }
+        const float2 a01 = ptx::add2(acc[0], acc[1]);
+        const float2 a23 = ptx::add2(acc[2], acc[3]);
+        const float2 a = ptx::add2(a01, a23);
         if (!first && __any_sync(0xffffffffu, resc)) {
-          // O and l were accumulated against the old max: bring them to the new one.
-          const float alpha = resc ? ptx::ex2_approx(m - m_new) : 1.0f;
+          // O and l were accumulated against the old max: bring them to the new one
+          // (after the scores are consumed, so their registers are free).
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t v[32];
@@ -416,33 +457,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
           }
           l *= alpha;
         }
-        m = m_new;
-        const float mref = (m == -INFINITY) ? 0.f : m;
-
-        // Pass 2: p = 2^(s*scale*log2e - m), row sum, P to shared memory as bf16.
-        float sum = 0.f;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t v[32];
-          __syncwarp();
-          ptx::tmem_ld32(tS + cc * 32, v);
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int k0 = cc * 32 + 2 * e;
-            const float p0 = k0 < limit ? ptx::ex2_approx(fmaf(__uint_as_float(v[2 * e]), sl2, -mref)) : 0.f;
-            const float p1 = k0 + 1 < limit ? ptx::ex2_approx(fmaf(__uint_as_float(v[2 * e + 1]), sl2, -mref)) : 0.f;
-            sum += p0 + p1;
-            w[e] = ptx::pack_bf16x2(p0, p1);
-          }
-          const uint32_t line = prow + (uint32_t)(cc >> 1) * kHalfBytes;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t chunk = (uint32_t)((cc & 1) * 4 + j);
-            ptx::st_shared_v4(line + ((chunk ^ rsw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          }
-        }
-        l += sum;
+        l += a.x + a.y;
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c.bar(kPFull + g));
@@ -504,16 +519,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + kOffSlot);
 
   ProducerState ps{0u, 0u};
-  if (warp == 0) {
-    if (lane == 0) run_producer(P, c, sbase, &tq, &tk, &tv, ps);
-  } else if (warp == 1) {
-    if (lane == 0) {
-      run_mma(P, c, sbase, tmem);
-      // Every MMA this thread issued must retire before TMEM is freed.
-      ptx::mma_commit(c.bar(kDone));
-      drain_bar(c, c.bar(kDone), 0);
+  if (warp < 4) {
+    ptx::regs_release<kRegsOther>();
+    if (warp == 0) {
+      if (lane == 0) run_producer(P, c, sbase, &tq, &tk, &tv, ps);
+    } else if (warp == 1) {
+      if (lane == 0) {
+        run_mma(P, c, sbase, tmem);
+        // Every MMA this thread issued must retire before TMEM is freed.
+        ptx::mma_commit(c.bar(kDone));
+        drain_bar(c, c.bar(kDone), 0);
+      }
     }
-  } else if (warp >= 4) {
+  } else {
+    ptx::regs_acquire<kRegsSoftmax>();
     run_softmax(P, c, sbase, tmem, (warp - 4) >> 2, warp & 3, lane);
   }
 
@@ -580,8 +599,18 @@ cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, 
     *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_bf16_kernel);
+  if (e != cudaSuccess) {
+    *why = "cudaFuncGetAttributes failed";
+    return e;
+  }
+  // setmaxnreg.inc waits until the registers exist: only launch when the split fits.
+  if ((uint32_t)attr.numRegs * kThreads < 128 * kRegsOther + 256 * kRegsSoftmax) {
+    *why = "kernel was built with fewer launch registers than its warpgroup split needs";
+    return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
