@@ -194,17 +194,21 @@ def run_ours(args, wl):
     stream = torch.cuda.current_stream()
     launches_per_step = 6
 
-    def step(fwd_events=None):
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         ra.ra_layout_perm(q, layout, N, out=ql)
         ra.ra_layout_perm(k, layout, N, out=kl)
         ra.ra_layout_perm(v, layout, N, out=vl)
-        if fwd_events is not None:
-            fwd_events[0].record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         ra.ra_fwd(plan, ql, kl, vl, o=o_l, lse=lse_l)
-        if fwd_events is not None:
-            fwd_events[1].record(stream)
+        if ev is not None:
+            ev[2].record(stream)
         ra.ra_layout_perm(o_l, layout, N, inverse=True, out=o_n)
         ra.ra_layout_perm(lse_l, layout, N, inverse=True, out=lse_n)
+        if ev is not None:
+            ev[3].record(stream)
 
     def barrier():
         if pg is not None:
@@ -215,8 +219,7 @@ def run_ours(args, wl):
         step()
     ra.ra_sync_status(plan)
 
-    fwd_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+    fwd_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(local) as clk:
@@ -227,7 +230,9 @@ def run_ours(args, wl):
         barrier()
     ra.ra_sync_status(plan)
     total_ms = start.elapsed_time(end)
-    fwd_ms = [a.elapsed_time(b) for a, b in fwd_ev]
+    fwd_ms = [e[1].elapsed_time(e[2]) for e in fwd_ev]
+    perm_in_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in fwd_ev)
+    perm_out_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in fwd_ev)
     if pg is not None:
         t = torch.tensor([total_ms, max(fwd_ms)], device=dev)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -270,6 +275,16 @@ def run_ours(args, wl):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         ra.ra_sync_status(plan)
 
+    kernels = None
+    if not args.no_kernels:
+        bytes_in = 2 * sum(t.numel() * t.element_size() for t in (q, k, v))
+        bytes_out = 2 * (o_n.numel() * o_n.element_size() + lse_n.numel() * lse_n.element_size())
+        kernels = {
+            "layout_perm_in": {"ms": perm_in_ms, "bytes": bytes_in, "GB/s": bytes_in / perm_in_ms / 1e6},
+            "layout_perm_out": {"ms": perm_out_ms, "bytes": bytes_out, "GB/s": bytes_out / perm_out_ms / 1e6},
+            "merge": merge_bandwidth(ra, torch, dev, stream),
+        }
+
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
@@ -305,7 +320,12 @@ def run_ours(args, wl):
         "tile_counts": {"full": full.tolist(), "partial": part.tolist(), "skip": skip.tolist(),
                         "granularity": "128x128 per (batch, query head)"},
         "algorithmic_flops_per_step": flops,
+        "kernels": kernels,
     }
+    if kernels is not None:
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        for kv in kernels.values():
+            kv["frac_of_hbm"] = kv["GB/s"] / hbm
     if world == 1 and not args.no_cpu_baseline:
         v_cpu, dt, _, desc = cpu_oracle_sample(wl, rows=args.ref_rows)
         line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
@@ -316,19 +336,45 @@ def run_ours(args, wl):
     return 0
 
 
+def merge_bandwidth(ra, torch, dev, stream, n_parts=8, rows=1 << 20, d=128, reps=5):
+    """ra_merge_partials on 8 synthetic float32 parts of 1M rows x 128 -> bf16 (HBM-bound)."""
+    g = torch.Generator(device=dev).manual_seed(77)
+    o_parts = torch.randn((n_parts, rows, d), generator=g, device=dev)
+    lse_parts = torch.randn((n_parts, rows), generator=g, device=dev)
+    o = torch.empty((rows, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((rows,), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        ra.ra_merge_partials(o_parts, lse_parts, o=o, lse=lse)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        ra.ra_merge_partials(o_parts, lse_parts, o=o, lse=lse)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    nbytes = n_parts * rows * (4 * d + 4) + rows * (2 * d + 4)
+    return {"ms": ms, "bytes": nbytes, "GB/s": nbytes / ms / 1e6,
+            "shape": f"{n_parts} parts x {rows} rows x {d} f32 -> bf16 (working set > L2)"}
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="zigzag_1m_n8")
+    ap.add_argument("--layout", default=None, help="override the workload's layout")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernels", action="store_true", help="skip the permute/merge bandwidth lines")
     args = ap.parse_args()
     from context_ring_attention_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
+    if args.layout:
+        import dataclasses
+        wl = dataclasses.replace(wl, layouts=(args.layout,))
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -10,15 +10,18 @@
 //
 // How (one persistent CTA per SM, 12 warps):
 //   warp 0     TMA producer: Q tiles once per work item, then K and V tiles in
-//              ring order into a 3-slot shared-memory ring (128B swizzle).
-//   warp 1     tcgen05 issuer: S = Q K^T into TMEM, O += P V into TMEM.
+//              ring order into a 5-slot shared-memory ring (128B swizzle).
+//   warp 1     tcgen05 issuer (whole warp, one elected lane issues): S = Q K^T into TMEM (both operands in shared
+//              memory), O += P V into TMEM (P read from TMEM, V from shared memory).
 //   warps 4-7  softmax for query tile 0, warps 8-11 for query tile 1: one thread
 //              per row reads its 128 scores from TMEM in one round trip, updates
-//              m and l, writes P (bf16) to shared memory, rescales O in TMEM when
-//              m moves, and writes O / l and the LSE at the end of a segment.
+//              m and l, writes P (bf16) back into the upper half of its S columns,
+//              rescales O in TMEM when m moves, and writes O / l and the LSE at the
+//              end of a segment.
 //   Warpgroup 0 (warps 0-3) hands registers to the softmax warpgroups (setmaxnreg).
 // Two query tiles per CTA let one tile's softmax overlap the other tile's MMAs.
-// TMEM: S0 cols 0-127, S1 128-255, O0 256-383, O1 384-511 (all 512 columns).
+// TMEM: S0 cols 0-127 (P0 in 64-127), S1 128-255 (P1 in 192-255), O0 256-383,
+// O1 384-511 (all 512 columns).
 //
 // Every mbarrier wait is bounded (~1 s).  On expiry the CTA raises an abort flag,
 // records the role in the plan's status word, drains its own in-flight TMA
@@ -44,11 +47,10 @@ constexpr uint32_t kRegsSoftmax = 192;
 static_assert(128 * kRegsOther + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile
 constexpr uint32_t kHalfBytes = 128 * 64 * 2;   // 128 rows x one 128-byte swizzle column
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr uint32_t kOffQ = 0;                            // Q0, Q1
 constexpr uint32_t kOffKV = 2 * kTileBytes;              // K/V ring
-constexpr uint32_t kOffP = kOffKV + kStages * kTileBytes;  // P0, P1
-constexpr uint32_t kOffBar = kOffP + 2 * kTileBytes;
+constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
 
 enum : int {
   kQFull = 0,
@@ -69,10 +71,18 @@ static_assert(8 * kNumBars + 8 <= 256, "barrier area");
 constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int g) { return g ? 128u : 0u; }
 __device__ __forceinline__ uint32_t col_o(int g) { return g ? 384u : 256u; }
+// P (bf16, two per 32-bit column) overwrites the upper half of its tile's S columns
+// once the softmax has read S; the next S MMA of that tile is issued after the PV
+// MMA that reads P.
+constexpr uint32_t kColP = 64;
 
 constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 128, false, true);  // V is MN-major
 constexpr uint64_t kWaitBudgetNs = 1000000000ull;
+#ifndef RA_SUSPEND_HINT_NS
+#define RA_SUSPEND_HINT_NS 2000u
+#endif
+constexpr uint32_t kSuspendHintNs = RA_SUSPEND_HINT_NS;  // a waiting thread sleeps up to this long per try
 constexpr float kRescaleSlack = 8.0f;  // log2 units: keep a stale max while p <= 2^8
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -88,8 +98,8 @@ __device__ __forceinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t pa
   if (ptx::mbar_test(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_test(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    if (ptx::mbar_wait_hint(bar, parity, kSuspendHintNs)) return true;
+    if ((it & 15u) == 0) {
       if (*c.abort) return false;
       if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
         *c.abort = 1u;
@@ -189,55 +199,62 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase,
 }
 
 // ----------------------------------------------------------------------- MMA --
-__device__ __forceinline__ void issue_s(uint32_t sbase, uint32_t tmem, int g, uint32_t ks) {
-  const uint32_t a0 = sbase + kOffQ + (uint32_t)g * kTileBytes;
-  const uint32_t b0 = sbase + kOffKV + ks * kTileBytes;
+// Descriptor low words of the tiles the MMA thread reads (see ptx::desc_lo).
+struct Descs {
+  uint32_t q0;  // Q0 (K-major); Q1 follows one tile later
+  uint32_t k0;  // K/V ring slot 0 as a K-major operand (K)
+  uint32_t v0;  // slot 0 as an MN-major operand (V); slot s adds s tiles
+};
+constexpr uint32_t kTileDesc = kTileBytes >> 4;  // one tile in descriptor address units
+
+__device__ __forceinline__ void issue_s(const Descs& dl, uint32_t tmem, int g, uint32_t ks) {
+  const uint32_t a0 = dl.q0 + (uint32_t)g * kTileDesc, b0 = dl.k0 + ks * kTileDesc;
 #pragma unroll
   for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of K = 16 over d = 128
-    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3u) * 32u;
-    ptx::mma_bf16_ss(tmem + col_s(g), ptx::sw128_desc(a0 + off, 16, 1024),
-                     ptx::sw128_desc(b0 + off, 16, 1024), kIdescS, kk > 0);
+    const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3u) * 32u) >> 4;
+    ptx::mma_bf16_ss_lo_warp(tmem + col_s(g), a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t sbase, uint32_t tmem, int g, uint32_t vs,
-                                         bool accumulate) {
-  const uint32_t a0 = sbase + kOffP + (uint32_t)g * kTileBytes;
-  const uint32_t b0 = sbase + kOffKV + vs * kTileBytes;
+__device__ __forceinline__ void issue_pv(const Descs& dl, uint32_t tmem, int g, uint32_t vs, bool accumulate) {
+  const uint32_t a0 = tmem + col_s(g) + kColP;  // P in tensor memory
+  const uint32_t b0 = dl.v0 + vs * kTileDesc;
 #pragma unroll
-  for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of 16 keys
-    const uint32_t a_off = (kk >> 2) * kHalfBytes + (kk & 3u) * 32u;
+  for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of 16 keys = 8 TMEM columns of P
     // V is [keys][d]: 16 keys = 2 groups of 8 rows (SBO 1 KiB); d halves 16 KiB apart (LBO).
-    ptx::mma_bf16_ss(tmem + col_o(g), ptx::sw128_desc(a0 + a_off, 16, 1024),
-                     ptx::sw128_desc(b0 + kk * 2048u, kHalfBytes, 1024), kIdescPV,
-                     (accumulate || kk > 0) ? 1u : 0u);
+    ptx::mma_bf16_ts_lo_warp(tmem + col_o(g), a0 + kk * 8u, b0 + ((kk * 2048u) >> 4), kIdescPV,
+                        (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
 __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32_t tmem) {
   const bool partials = P.o_parts != nullptr;
+  Descs dl;
+  dl.q0 = ptx::desc_lo(sbase + kOffQ, 16);
+  dl.k0 = ptx::desc_lo(sbase + kOffKV, 16);
+  dl.v0 = ptx::desc_lo(sbase + kOffKV, kHalfBytes);
   uint32_t kv_it = 0, u = 0, pj0 = 0, pj1 = 0;
   for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x, ++u) {
     const WorkItem it = P.items[idx];
     const bool two = it.bh1 >= 0;
-    if (!wait_bar(c, c.bar(kQFull), u & 1u, kStatusTimeoutMma)) return;
-    ptx::tc_fence_after();
+    // Waits on TMA-filled buffers need no tcgen05 fence: the mbarrier completion
+    // already orders the async-proxy writes before the MMAs that read them.
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kQFull), u & 1u, kStatusTimeoutMma))) return;
     Walk cur;
     walk_begin(cur, P, it.shard, it.maxq);
     if (cur.t >= P.n_shards) {
-      ptx::mma_commit(c.bar(kQEmpty));
+      ptx::mma_commit_warp(c.bar(kQEmpty));
       continue;
     }
     uint32_t ks = kv_it % kStages;
-    if (!wait_bar(c, c.bar(kKVFull + ks), (kv_it / kStages) & 1u, kStatusTimeoutMma)) return;
-    ptx::tc_fence_after();
-    issue_s(sbase, tmem, 0, ks);
-    ptx::mma_commit(c.bar(kSFull + 0));
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kKVFull + ks), (kv_it / kStages) & 1u, kStatusTimeoutMma))) return;
+    issue_s(dl, tmem, 0, ks);
+    ptx::mma_commit_warp(c.bar(kSFull + 0));
     if (two) {
-      issue_s(sbase, tmem, 1, ks);
-      ptx::mma_commit(c.bar(kSFull + 1));
+      issue_s(dl, tmem, 1, ks);
+      ptx::mma_commit_warp(c.bar(kSFull + 1));
     }
-    ptx::mma_commit(c.bar(kKVEmpty + ks));
+    ptx::mma_commit_warp(c.bar(kKVEmpty + ks));
     ++kv_it;
     bool first_tile = true;
     for (;;) {
@@ -247,40 +264,40 @@ __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32
       const bool seg_first = partials ? (cur.kt == 0) : first_tile;
       const bool seg_last = partials ? (!has_next || nxt.t != cur.t) : !has_next;
       const uint32_t vs = kv_it % kStages;
-      if (!wait_bar(c, c.bar(kKVFull + vs), (kv_it / kStages) & 1u, kStatusTimeoutMma)) return;
+      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kKVFull + vs), (kv_it / kStages) & 1u, kStatusTimeoutMma))) return;
       ++kv_it;
-      if (!wait_bar(c, c.bar(kPFull + 0), pj0 & 1u, kStatusTimeoutMma)) return;
+      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kPFull + 0), pj0 & 1u, kStatusTimeoutMma))) return;
       ++pj0;
       ptx::tc_fence_after();
-      issue_pv(sbase, tmem, 0, vs, !seg_first);
-      if (seg_last) ptx::mma_commit(c.bar(kOFull + 0));
+      issue_pv(dl, tmem, 0, vs, !seg_first);
+      if (seg_last) ptx::mma_commit_warp(c.bar(kOFull + 0));
       uint32_t ks2 = 0;
       if (has_next) {
         ks2 = kv_it % kStages;
-        if (!wait_bar(c, c.bar(kKVFull + ks2), (kv_it / kStages) & 1u, kStatusTimeoutMma)) return;
+        if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kKVFull + ks2), (kv_it / kStages) & 1u, kStatusTimeoutMma))) return;
         ptx::tc_fence_after();
-        issue_s(sbase, tmem, 0, ks2);
-        ptx::mma_commit(c.bar(kSFull + 0));
+        issue_s(dl, tmem, 0, ks2);
+        ptx::mma_commit_warp(c.bar(kSFull + 0));
       }
       if (two) {
-        if (!wait_bar(c, c.bar(kPFull + 1), pj1 & 1u, kStatusTimeoutMma)) return;
+        if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kPFull + 1), pj1 & 1u, kStatusTimeoutMma))) return;
         ++pj1;
         ptx::tc_fence_after();
-        issue_pv(sbase, tmem, 1, vs, !seg_first);
-        if (seg_last) ptx::mma_commit(c.bar(kOFull + 1));
+        issue_pv(dl, tmem, 1, vs, !seg_first);
+        if (seg_last) ptx::mma_commit_warp(c.bar(kOFull + 1));
       }
-      ptx::mma_commit(c.bar(kKVEmpty + vs));
+      ptx::mma_commit_warp(c.bar(kKVEmpty + vs));
       if (!has_next) break;
       if (two) {
-        issue_s(sbase, tmem, 1, ks2);
-        ptx::mma_commit(c.bar(kSFull + 1));
+        issue_s(dl, tmem, 1, ks2);
+        ptx::mma_commit_warp(c.bar(kSFull + 1));
       }
-      ptx::mma_commit(c.bar(kKVEmpty + ks2));
+      ptx::mma_commit_warp(c.bar(kKVEmpty + ks2));
       ++kv_it;
       cur = nxt;
       first_tile = false;
     }
-    ptx::mma_commit(c.bar(kQEmpty));
+    ptx::mma_commit_warp(c.bar(kQEmpty));
   }
 }
 
@@ -334,8 +351,6 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + col_s(g);
   const uint32_t tO = tmem + lane_off + col_o(g);
-  const uint32_t prow = sbase + kOffP + (uint32_t)g * kTileBytes + (uint32_t)row * 128u;
-  const uint32_t rsw = (uint32_t)row & 7u;
   const bool partials = P.o_parts != nullptr;
   const int N = P.n_shards;
   const int64_t rows_all = (int64_t)P.batch * P.heads_q * P.seq;
@@ -416,30 +431,21 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
         m = m_new;
         const float mref = (m == -INFINITY) ? 0.f : m;
 
-        // p = 2^(s*scale*log2e - m) (masked -inf -> 0), row sum, P to shared memory as bf16.
+        // p = 2^(s*scale*log2e - m) (masked -inf -> 0), row sum, P to tensor memory as bf16.
         const float2 sc2 = make_float2(sl2, sl2);
         const float2 neg = make_float2(-mref, -mref);
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};
+        // Packed P word e overwrites register e, whose score was already consumed.
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int k0 = cc * 32 + 2 * e;
-            float2 x = ptx::fma2(make_float2(s[k0], s[k0 + 1]), sc2, neg);
-            x.x = ptx::ex2_approx(x.x);
-            x.y = ptx::ex2_approx(x.y);
-            acc[e & 3] = ptx::add2(acc[e & 3], x);
-            w[e] = ptx::pack_bf16x2(x.x, x.y);
-          }
-          const uint32_t line = prow + (uint32_t)(cc >> 1) * kHalfBytes;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t chunk = (uint32_t)((cc & 1) * 4 + j);
-            ptx::st_shared_v4(line + ((chunk ^ rsw) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-          }
+        for (int e = 0; e < 64; ++e) {
+          float2 x = ptx::fma2(make_float2(s[2 * e], s[2 * e + 1]), sc2, neg);
+          x.x = ptx::ex2_approx(x.x);
+          x.y = ptx::ex2_approx(x.y);
+          acc[e & 3] = ptx::add2(acc[e & 3], x);
+          raw[e] = ptx::pack_bf16x2(x.x, x.y);
         }
+        ptx::tmem_st64(tS + kColP, *reinterpret_cast<const uint32_t(*)[64]>(raw));
         const float2 a01 = ptx::add2(acc[0], acc[1]);
         const float2 a23 = ptx::add2(acc[2], acc[3]);
         const float2 a = ptx::add2(a01, a23);
@@ -458,7 +464,6 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
           l *= alpha;
         }
         l += a.x + a.y;
-        ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         ptx::mbar_arrive(c.bar(kPFull + g));
 
@@ -524,12 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       if (lane == 0) run_producer(P, c, sbase, &tq, &tk, &tv, ps);
     } else if (warp == 1) {
-      if (lane == 0) {
-        run_mma(P, c, sbase, tmem);
-        // Every MMA this thread issued must retire before TMEM is freed.
-        ptx::mma_commit(c.bar(kDone));
-        drain_bar(c, c.bar(kDone), 0);
-      }
+      // The whole warp runs the MMA loop with warp-uniform values; one elected
+      // lane issues each tcgen05 instruction.
+      run_mma(P, c, sbase, tmem);
+      // Every MMA this warp issued must retire before TMEM is freed.
+      ptx::mma_commit_warp(c.bar(kDone));
+      drain_bar(c, c.bar(kDone), 0);
+      __syncwarp();
     }
   } else {
     ptx::regs_acquire<kRegsSoftmax>();

@@ -7,7 +7,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/ra.h"
+#include "ra.h"
 
 #ifdef __CUDACC__
 #define RA_HD __host__ __device__ __forceinline__
