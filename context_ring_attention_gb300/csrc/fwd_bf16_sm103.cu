@@ -11,8 +11,11 @@
 // How (one persistent CTA per SM, 12 warps):
 //   warp 0     TMA producer: Q tiles once per work item, then K and V tiles in
 //              ring order into a 5-slot shared-memory ring (128B swizzle).
-//   warp 1     tcgen05 issuer (whole warp, one elected lane issues): S = Q K^T into TMEM (both operands in shared
-//              memory), O += P V into TMEM (P read from TMEM, V from shared memory).
+//   warp 1     tcgen05 issuer: S = Q K^T into TMEM (both operands in shared
+//              memory), O += P V into TMEM (P from TMEM, V from shared memory).
+//   Warps 0 and 1 run converged with warp-uniform operands and one elected lane
+//   issues each instruction: a single divergent lane issues MMAs too slowly to
+//   keep the tensor pipe fed while the softmax warps share its scheduler.
 //   warps 4-7  softmax for query tile 0, warps 8-11 for query tile 1: one thread
 //              per row reads its 128 scores from TMEM in one round trip, updates
 //              m and l, writes P (bf16) back into the upper half of its S columns,
@@ -158,16 +161,16 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase,
   uint32_t kv_it = 0, u = 0;
   for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x, ++u) {
     const WorkItem it = P.items[idx];
-    if (!wait_bar(c, c.bar(kQEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer)) break;
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kQEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
     const bool two = it.bh1 >= 0;
-    ptx::mbar_arrive_expect_tx(c.bar(kQFull), (two ? 2u : 1u) * kTileBytes);
+    ptx::mbar_arrive_expect_tx_warp(c.bar(kQFull), (two ? 2u : 1u) * kTileBytes);
     const int32_t y0 = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
-    ptx::tma_load_2d(sbase + kOffQ, tq, c.bar(kQFull), 0, y0);
-    ptx::tma_load_2d(sbase + kOffQ + kHalfBytes, tq, c.bar(kQFull), 64, y0);
+    ptx::tma_load_2d_warp(sbase + kOffQ, tq, c.bar(kQFull), 0, y0);
+    ptx::tma_load_2d_warp(sbase + kOffQ + kHalfBytes, tq, c.bar(kQFull), 64, y0);
     if (two) {
       const int32_t y1 = (int32_t)((int64_t)it.bh1 * P.seq + (int64_t)it.shard * P.s_n + it.row1);
-      ptx::tma_load_2d(sbase + kOffQ + kTileBytes, tq, c.bar(kQFull), 0, y1);
-      ptx::tma_load_2d(sbase + kOffQ + kTileBytes + kHalfBytes, tq, c.bar(kQFull), 64, y1);
+      ptx::tma_load_2d_warp(sbase + kOffQ + kTileBytes, tq, c.bar(kQFull), 0, y1);
+      ptx::tma_load_2d_warp(sbase + kOffQ + kTileBytes + kHalfBytes, tq, c.bar(kQFull), 64, y1);
     }
     st.q_issued = u + 1;
     const int b = it.bh0 / P.heads_q;
@@ -181,15 +184,15 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase,
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // K tile, then V tile
         const uint32_t s = kv_it % kStages, use = kv_it / kStages;
-        if (!wait_bar(c, c.bar(kKVEmpty + s), (use & 1u) ^ 1u, kStatusTimeoutProducer)) {
+        if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kKVEmpty + s), (use & 1u) ^ 1u, kStatusTimeoutProducer))) {
           ok = false;
           break;
         }
         const uint32_t dst = sbase + kOffKV + s * kTileBytes;
         const CUtensorMap* map = which ? tv : tk;
-        ptx::mbar_arrive_expect_tx(c.bar(kKVFull + s), kTileBytes);
-        ptx::tma_load_2d(dst, map, c.bar(kKVFull + s), 0, y);
-        ptx::tma_load_2d(dst + kHalfBytes, map, c.bar(kKVFull + s), 64, y);
+        ptx::mbar_arrive_expect_tx_warp(c.bar(kKVFull + s), kTileBytes);
+        ptx::tma_load_2d_warp(dst, map, c.bar(kKVFull + s), 0, y);
+        ptx::tma_load_2d_warp(dst + kHalfBytes, map, c.bar(kKVFull + s), 64, y);
         st.kv_issued = ++kv_it;
       }
       walk_advance(w, P, it.shard, it.maxq);
@@ -527,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     ptx::regs_release<kRegsOther>();
     if (warp == 0) {
-      if (lane == 0) run_producer(P, c, sbase, &tq, &tk, &tv, ps);
+      run_producer(P, c, sbase, &tq, &tk, &tv, ps);  // whole warp; one elected lane issues
+      __syncwarp();
     } else if (warp == 1) {
       // The whole warp runs the MMA loop with warp-uniform values; one elected
       // lane issues each tcgen05 instruction.
@@ -542,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     run_softmax(P, c, sbase, tmem, (warp - 4) >> 2, warp & 3, lane);
   }
 
-  if (warp == 0 && lane == 0 && *c.abort) {
+  if (warp == 0 && lane == 0 && *c.abort) {  // (every lane of warp 0 holds the same counts)
     // Let this CTA's own TMA loads land before its shared memory goes away.
     for (uint32_t s = 0; s < (uint32_t)kStages; ++s) {
       if (ps.kv_issued > s) {
