@@ -452,6 +452,12 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
         const float2 a01 = ptx::add2(acc[0], acc[1]);
         const float2 a23 = ptx::add2(acc[2], acc[3]);
         const float2 a = ptx::add2(a01, a23);
+        // The PV MMA weighs each key by its bf16-rounded p while l sums the fp32 p.
+        // Replace the tile's largest p by its rounded value in l as well: when one
+        // key dominates a row, its rounding then cancels in o / l.
+        const float p_top = ptx::ex2_approx(fmaf(mx, sl2, -mref));
+        const float p_top_bf = __uint_as_float(ptx::pack_bf16x2(p_top, 0.f) << 16);
+        const float top_fix = p_top_bf - p_top;
         if (!first && __any_sync(0xffffffffu, resc)) {
           // O and l were accumulated against the old max: bring them to the new one
           // (after the scores are consumed, so their registers are free).
@@ -466,7 +472,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
           }
           l *= alpha;
         }
-        l += a.x + a.y;
+        l += (a.x + a.y) + top_fix;
         ptx::tc_fence_before();
         ptx::mbar_arrive(c.bar(kPFull + g));
 
