@@ -64,12 +64,17 @@ enum : int {
   kPFull = kSFull + 2,
   kOFull = kPFull + 2,
   kDone = kOFull + 2,
-  kNumBars = kDone + 1
+  kItemFull = kDone + 1,
+  kItemEmpty = kItemFull + 4,
+  kNumBars = kItemEmpty + 4
 };
+constexpr int kItemSlots = 4;          // work-item indices handed from the producer to the other roles
+constexpr uint32_t kItemConsumers = 9;  // MMA warp + 8 softmax warps
 constexpr uint32_t kOffSlot = kOffBar + 8 * kNumBars;  // TMEM base written by tcgen05.alloc
 constexpr uint32_t kOffAbort = kOffSlot + 4;
+constexpr uint32_t kOffItems = kOffAbort + 4;  // kItemSlots int32 item indices
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + slack to align the base to 1 KiB
-static_assert(8 * kNumBars + 8 <= 256, "barrier area");
+static_assert(8 * kNumBars + 8 + 4 * kItemSlots <= 256, "barrier area");
 
 constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int g) { return g ? 128u : 0u; }
@@ -149,17 +154,48 @@ __device__ __forceinline__ void walk_advance(Walk& w, const FwdParams& P, int p,
   if (++w.kt >= w.nt) walk_to_next_step(w, P, p, maxq);
 }
 
+// ------------------------------------------------------------- work items --
+// Items are handed out dynamically: the producer warp takes the next index of the
+// (longest-first, key/value-head-grouped) list from a global counter and passes it
+// to the other roles through a small ring in shared memory.  The items in flight
+// across the GPU are then always neighbours in the list, so the CTAs running
+// together share K/V tiles in L2, and the grid ends evenly.
+
+// Consumer side: index of this role's u-th item, or -1 at the end / on abort.
+__device__ __forceinline__ int next_item(const Ctl& c, volatile int32_t* slots, uint32_t u, int lane) {
+  const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
+  if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kItemFull + (int)slot), use & 1u, kStatusTimeoutSoftmax)))
+    return -1;
+  const int idx = slots[slot];
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(c.bar(kItemEmpty + (int)slot));
+  return idx;
+}
+
 // ------------------------------------------------------------------ producer --
 struct ProducerState {
   uint32_t kv_issued;
   uint32_t q_issued;
 };
 
-__device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase,
+__device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
                              const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              ProducerState& st) {
-  uint32_t kv_it = 0, u = 0;
-  for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x, ++u) {
+  uint32_t kv_it = 0;
+  const int lane = threadIdx.x & 31;
+  for (uint32_t u = 0;; ++u) {
+    // Publish the next item index (or -1 at the end) to the other roles.
+    const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kItemEmpty + (int)slot), (use & 1u) ^ 1u, kStatusTimeoutProducer)))
+      break;
+    int idx = 0;
+    if (lane == 0) idx = (int)atomicAdd(P.item_counter, 1u);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    if (idx >= P.n_items) idx = -1;
+    if (lane == 0) slots[slot] = idx;
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
+    if (idx < 0) break;
     const WorkItem it = P.items[idx];
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kQEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
     const bool two = it.bh1 >= 0;
@@ -230,14 +266,17 @@ __device__ __forceinline__ void issue_pv(const Descs& dl, uint32_t tmem, int g, 
   }
 }
 
-__device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32_t tmem) {
+__device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots, uint32_t tmem) {
   const bool partials = P.o_parts != nullptr;
   Descs dl;
   dl.q0 = ptx::desc_lo(sbase + kOffQ, 16);
   dl.k0 = ptx::desc_lo(sbase + kOffKV, 16);
   dl.v0 = ptx::desc_lo(sbase + kOffKV, kHalfBytes);
-  uint32_t kv_it = 0, u = 0, pj0 = 0, pj1 = 0;
-  for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x, ++u) {
+  uint32_t kv_it = 0, pj0 = 0, pj1 = 0;
+  const int lane = threadIdx.x & 31;
+  for (uint32_t u = 0;; ++u) {
+    const int idx = next_item(c, slots, u, lane);
+    if (idx < 0) break;
     const WorkItem it = P.items[idx];
     const bool two = it.bh1 >= 0;
     // Waits on TMA-filled buffers need no tcgen05 fence: the mbarrier completion
@@ -348,8 +387,8 @@ __device__ __forceinline__ void store_segment(const FwdParams& P, uint32_t tO, f
   }
 }
 
-__device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, uint32_t tmem, int g,
-                            int wq, int lane) {
+__device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
+                            uint32_t tmem, int g, int wq, int lane) {
   const int row = wq * 32 + lane;  // TMEM lane = query row of the tile
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + col_s(g);
@@ -360,7 +399,9 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, ui
   const float sl2 = P.scale_log2;
   uint32_t sj = 0, oj = 0;
 
-  for (int idx = blockIdx.x; idx < P.n_items; idx += gridDim.x) {
+  for (uint32_t u = 0;; ++u) {
+    const int idx = next_item(c, slots, u, lane);
+    if (idx < 0) break;
     const WorkItem it = P.items[idx];
     if (g == 1 && it.bh1 < 0) continue;
     const int bh = g ? it.bh1 : it.bh0;
@@ -501,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sgen = smem_raw + (sbase - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Ctl c{sbase + kOffBar, reinterpret_cast<volatile uint32_t*>(sgen + kOffAbort), P.status};
+  volatile int32_t* slots = reinterpret_cast<volatile int32_t*>(sgen + kOffItems);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(c.bar(kQFull), 1);
@@ -515,6 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(c.bar(kOFull + g), 1);
     }
     ptx::mbar_init(c.bar(kDone), 1);
+    for (int s2 = 0; s2 < kItemSlots; ++s2) {
+      ptx::mbar_init(c.bar(kItemFull + s2), 1);
+      ptx::mbar_init(c.bar(kItemEmpty + s2), kItemConsumers);
+    }
     *c.abort = 0u;
     ptx::fence_barrier_init();
   }
@@ -536,12 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     ptx::regs_release<kRegsOther>();
     if (warp == 0) {
-      run_producer(P, c, sbase, &tq, &tk, &tv, ps);  // whole warp; one elected lane issues
+      run_producer(P, c, sbase, slots, &tq, &tk, &tv, ps);  // whole warp; one elected lane issues
       __syncwarp();
     } else if (warp == 1) {
       // The whole warp runs the MMA loop with warp-uniform values; one elected
       // lane issues each tcgen05 instruction.
-      run_mma(P, c, sbase, tmem);
+      run_mma(P, c, sbase, slots, tmem);
       // Every MMA this warp issued must retire before TMEM is freed.
       ptx::mma_commit_warp(c.bar(kDone));
       drain_bar(c, c.bar(kDone), 0);
@@ -549,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     ptx::regs_acquire<kRegsSoftmax>();
-    run_softmax(P, c, sbase, tmem, (warp - 4) >> 2, warp & 3, lane);
+    run_softmax(P, c, sbase, slots, tmem, (warp - 4) >> 2, warp & 3, lane);
   }
 
   if (warp == 0 && lane == 0 && *c.abort) {  // (every lane of warp 0 holds the same counts)

@@ -64,7 +64,7 @@ ra_status check_problem(const ra_problem* p) {
   return RA_OK;
 }
 
-// The planner's work list (same items, same longest-first order), written into
+// The planner's work list (same items, same schedule order), written into
 // the static host buffer.  Returns the item count, or -1 when it would not fit.
 int64_t build_items(const ra_problem& pb) {
   const int N = pb.n_shards;
@@ -101,8 +101,13 @@ int64_t build_items(const ra_problem& pb) {
           g_host_items[n] = {w, n};
           ++n;
         }
-  std::sort(g_host_items, g_host_items + n, [](const Keyed& a, const Keyed& b) {
-    return a.w.cost != b.w.cost ? a.w.cost > b.w.cost : a.order < b.order;
+  int64_t max_cost = 1;
+  for (int64_t i = 0; i < n; ++i) max_cost = std::max<int64_t>(max_cost, g_host_items[i].w.cost);
+  const int64_t width = ra::schedule_bucket_width(max_cost);
+  const int G = pb.heads_q / pb.heads_kv;
+  std::sort(g_host_items, g_host_items + n, [&](const Keyed& a, const Keyed& b) {
+    return ra::schedule_before(ra::schedule_key(a.w, pb.heads_q, G, width, a.order),
+                               ra::schedule_key(b.w, pb.heads_q, G, width, b.order));
   });
   return n;
 }
@@ -149,7 +154,8 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   // Pageable-source async copies return once the source has been staged, so the
   // static host buffer may be reused by the next call.
   cudaError_t e = cudaMemcpyAsync(d_items, packed, (size_t)n_items * sizeof(ra::WorkItem), cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, sizeof(uint32_t), st);  // status word starts clear
+  // status word and work-item counter start at zero
+  if (e == cudaSuccess) e = cudaMemsetAsync(base, 0, 2 * sizeof(uint32_t), st);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, cudaGetErrorString(e));
 
   ra::FwdParams prm{};
@@ -172,6 +178,7 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   prm.o_parts = nullptr;
   prm.lse_parts = nullptr;
   prm.status = reinterpret_cast<uint32_t*>(base);
+  prm.item_counter = reinterpret_cast<uint32_t*>(base) + 1;
   if (n_items == 0) return RA_OK;
   const int grid = (int)std::min<int64_t>(n_items, g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 148);
   const char* why = "";

@@ -163,12 +163,17 @@ void build_schedule(ra_plan_s* pl) {
       }
     }
   }
-  // Longest first; equal costs keep generation order (heads of one row tile adjacent,
-  // so concurrently running CTAs share key/value tiles through L2).
-  std::stable_sort(list.begin(), list.end(),
-                   [](const Keyed& a, const Keyed& b) { return a.w.cost > b.w.cost; });
+  int64_t max_cost = 1;
+  for (const Keyed& k : list) max_cost = std::max<int64_t>(max_cost, k.w.cost);
+  const int64_t width = ra::schedule_bucket_width(max_cost);
+  std::vector<ra::ScheduleKey> keys(list.size());
+  for (size_t n = 0; n < list.size(); ++n)
+    keys[n] = ra::schedule_key(list[n].w, pb.heads_q, G, width, list[n].order);
+  std::vector<size_t> idx(list.size());
+  for (size_t n = 0; n < idx.size(); ++n) idx[n] = n;
+  std::sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return ra::schedule_before(keys[a], keys[b]); });
   pl->items.resize(list.size());
-  for (size_t n = 0; n < list.size(); ++n) pl->items[n] = list[n].w;
+  for (size_t n = 0; n < list.size(); ++n) pl->items[n] = list[idx[n]].w;
 }
 
 ra_status upload(ra_plan_s* pl) {
@@ -289,6 +294,7 @@ ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, vo
   prm.o_parts = o_parts;
   prm.lse_parts = lse_parts;
   prm.status = plan->d_status;
+  prm.item_counter = plan->d_status + 1;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   cudaError_t e;
@@ -296,6 +302,9 @@ ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, vo
     if (prm.n_items == 0) return ok();
     const int grid = std::min(prm.n_items, plan->sm_count > 0 ? plan->sm_count : 148);
     const char* why = "";
+    // The kernel hands out work items from a counter that starts at zero.
+    e = cudaMemsetAsync(prm.item_counter, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
     e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   } else {

@@ -78,6 +78,26 @@ struct alignas(16) WorkItem {
   int32_t pad;
 };
 
+// Schedule order of work items for the persistent grid, which hands items out
+// round-robin: longest first (so the grid ends evenly), but items whose cost lies
+// in the same bucket of ~1% of the largest cost are ordered by (batch, key/value
+// head) first.  A round of items then mostly streams one key/value head, so the
+// CTAs that run together read the same K/V tiles and share them through L2.
+struct ScheduleKey {
+  int64_t bucket, kv, cost, seq;
+};
+inline ScheduleKey schedule_key(const WorkItem& w, int heads_q, int group, int64_t bucket_width, int64_t seq) {
+  const int64_t b = w.bh0 / heads_q, h = w.bh0 % heads_q;
+  return {w.cost / bucket_width, b * (heads_q / group) + h / group, w.cost, seq};
+}
+inline bool schedule_before(const ScheduleKey& a, const ScheduleKey& b) {
+  if (a.bucket != b.bucket) return a.bucket > b.bucket;
+  if (a.kv != b.kv) return a.kv < b.kv;
+  if (a.cost != b.cost) return a.cost > b.cost;
+  return a.seq < b.seq;
+}
+inline int64_t schedule_bucket_width(int64_t max_cost) { return max_cost >= 200 ? max_cost / 100 : 1; }
+
 struct FwdParams {
   int32_t batch, heads_q, heads_kv, group, head_dim, n_shards, layout, causal;
   int64_t seq, s_n;
@@ -89,7 +109,8 @@ struct FwdParams {
   float* lse;        // fused LSE or nullptr
   float* o_parts;    // partials mode outputs or nullptr
   float* lse_parts;
-  uint32_t* status;  // device status word (bit set = a wait ran out of budget)
+  uint32_t* status;        // device status word (bit set = a wait ran out of budget)
+  uint32_t* item_counter;  // next work item to hand out; zero before each launch
 };
 
 // Status bits written by kernels into the plan's status word.

@@ -131,7 +131,8 @@ ra_status ra_plan_tile_counts(ra_plan_t plan, int64_t* full, int64_t* partial, i
  *   key gives O_t = 0, LSE_t = -inf.  ra_merge_partials combines them.
  * Asynchronous on stream; allocates nothing.  A device-side wait that runs out
  * of budget makes the kernel return early and sets the plan's status word;
- * ra_sync_status reports it.
+ * ra_sync_status reports it.  Calls that share a plan must not overlap on the
+ * GPU (the plan's device words hold the status and the work-item counter).
  * Errors: RA_ERR_INVALID_ARG (null/misaligned pointers, mixed modes),
  * RA_ERR_NO_DEVICE, RA_ERR_CUDA (launch failure).
  */
