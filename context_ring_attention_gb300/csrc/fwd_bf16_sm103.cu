@@ -173,6 +173,8 @@ __device__ __forceinline__ int next_item(const Ctl& c, volatile int32_t* slots, 
 }
 
 // ------------------------------------------------------------------ producer --
+#define TMA_Q(d, m, b, x, y) ptx::tma_load_2d_warp_hint(d, m, b, x, y, once)
+#define TMA_KV(d, m, b, x, y) ptx::tma_load_2d_warp_hint(d, m, b, x, y, keep)
 struct ProducerState {
   uint32_t kv_issued;
   uint32_t q_issued;
@@ -183,6 +185,8 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
                              ProducerState& st) {
   uint32_t kv_it = 0;
   const int lane = threadIdx.x & 31;
+  const uint64_t keep = ptx::l2_policy_evict_last();   // K/V: re-read by the CTAs running together
+  const uint64_t once = ptx::l2_policy_evict_first();  // Q: read once
   for (uint32_t u = 0;; ++u) {
     // Publish the next item index (or -1 at the end) to the other roles.
     const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
@@ -201,12 +205,12 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
     const bool two = it.bh1 >= 0;
     ptx::mbar_arrive_expect_tx_warp(c.bar(kQFull), (two ? 2u : 1u) * kTileBytes);
     const int32_t y0 = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
-    ptx::tma_load_2d_warp(sbase + kOffQ, tq, c.bar(kQFull), 0, y0);
-    ptx::tma_load_2d_warp(sbase + kOffQ + kHalfBytes, tq, c.bar(kQFull), 64, y0);
+    TMA_Q(sbase + kOffQ, tq, c.bar(kQFull), 0, y0);
+    TMA_Q(sbase + kOffQ + kHalfBytes, tq, c.bar(kQFull), 64, y0);
     if (two) {
       const int32_t y1 = (int32_t)((int64_t)it.bh1 * P.seq + (int64_t)it.shard * P.s_n + it.row1);
-      ptx::tma_load_2d_warp(sbase + kOffQ + kTileBytes, tq, c.bar(kQFull), 0, y1);
-      ptx::tma_load_2d_warp(sbase + kOffQ + kTileBytes + kHalfBytes, tq, c.bar(kQFull), 64, y1);
+      TMA_Q(sbase + kOffQ + kTileBytes, tq, c.bar(kQFull), 0, y1);
+      TMA_Q(sbase + kOffQ + kTileBytes + kHalfBytes, tq, c.bar(kQFull), 64, y1);
     }
     st.q_issued = u + 1;
     const int b = it.bh0 / P.heads_q;
@@ -227,8 +231,8 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
         const uint32_t dst = sbase + kOffKV + s * kTileBytes;
         const CUtensorMap* map = which ? tv : tk;
         ptx::mbar_arrive_expect_tx_warp(c.bar(kKVFull + s), kTileBytes);
-        ptx::tma_load_2d_warp(dst, map, c.bar(kKVFull + s), 0, y);
-        ptx::tma_load_2d_warp(dst + kHalfBytes, map, c.bar(kKVFull + s), 64, y);
+        TMA_KV(dst, map, c.bar(kKVFull + s), 0, y);
+        TMA_KV(dst + kHalfBytes, map, c.bar(kKVFull + s), 64, y);
         st.kv_issued = ++kv_it;
       }
       walk_advance(w, P, it.shard, it.maxq);
