@@ -241,27 +241,62 @@ def run_ours(args, wl):
     flops = wl.flops()
     value = world * flops / (ms_per_step * 1e-3) / 1e12
 
-    # End to end through host buffers: H2D of natural-order Q/K/V, the step, D2H of O/LSE.
+    # End to end through host buffers: every step copies its natural-order Q/K/V in
+    # from pinned host memory and its O/LSE back out.  Steps are pipelined the way a
+    # serving loop runs: step i+1's inputs travel (H2D stream) while step i computes,
+    # and step i's outputs travel back (D2H stream) while step i+1 computes.
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
         ho = torch.empty(o_n.shape, dtype=o_n.dtype, pin_memory=True)
         hl = torch.empty(lse_n.shape, dtype=lse_n.dtype, pin_memory=True)
+        bufs = [(q, k, v, o_n, lse_n),
+                (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o_n),
+                 torch.empty_like(lse_n))]
+        h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        evs = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+        h2d_done, in_free, comp_done, d2h_done = evs(), evs(), evs(), evs()
 
-        def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            step()
-            ho.copy_(o_n, non_blocking=True)
-            hl.copy_(lse_n, non_blocking=True)
+        def h2d(slot):
+            for t_h, t_d in zip((hq, hk, hv), bufs[slot][:3]):
+                t_d.copy_(t_h, non_blocking=True)
+            h2d_done[slot].record(h2d_s)
 
-        e2e_step()
+        def run_pipeline(n):
+            with torch.cuda.stream(h2d_s):
+                h2d(0)
+            for i in range(n):
+                b = i % 2
+                bq, bk, bv, bo, bl = bufs[b]
+                stream.wait_event(h2d_done[b])       # this step's inputs have arrived
+                ra.ra_layout_perm(bq, layout, N, out=ql)
+                ra.ra_layout_perm(bk, layout, N, out=kl)
+                ra.ra_layout_perm(bv, layout, N, out=vl)
+                in_free[b].record(stream)
+                ra.ra_fwd(plan, ql, kl, vl, o=o_l, lse=lse_l)
+                if i >= 2:
+                    stream.wait_event(d2h_done[b])   # step i-2's outputs have left this slot
+                ra.ra_layout_perm(o_l, layout, N, inverse=True, out=bo)
+                ra.ra_layout_perm(lse_l, layout, N, inverse=True, out=bl)
+                comp_done[b].record(stream)
+                if i + 1 < n:
+                    with torch.cuda.stream(h2d_s):
+                        if i >= 1:
+                            h2d_s.wait_event(in_free[1 - b])  # step i-1 has read its inputs
+                        h2d(1 - b)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(comp_done[b])
+                    ho.copy_(bo, non_blocking=True)
+                    hl.copy_(bl, non_blocking=True)
+                    d2h_done[b].record(d2h_s)
+            stream.wait_stream(h2d_s)
+            stream.wait_stream(d2h_s)
+
+        run_pipeline(2)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        run_pipeline(args.steps)
         e1.record(stream)
         barrier()
         e_ms = e0.elapsed_time(e1) / args.steps
@@ -269,10 +304,11 @@ def run_ours(args, wl):
             t = torch.tensor([e_ms], device=dev)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
             e_ms = t.item()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        h2d_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h_bytes = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "note": "pinned host buffers, two device slots; H2D of step i+1 and D2H of step i-1 overlap step i"}
         ra.ra_sync_status(plan)
 
     kernels = None

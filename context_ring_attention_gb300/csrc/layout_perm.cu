@@ -35,12 +35,55 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// 256-byte rows (128 bf16 values, the attention case): a half-warp moves one
+// row as 16 x 16 B; each thread keeps kRowsPerThread rows in flight (all loads,
+// then all stores); row positions use 32-bit arithmetic once per row.
+constexpr int kRowsPerThread = 4;
+constexpr int kRowsPerPass = kThreads / 16;                      // 16 rows per block pass
+constexpr int kRowsPerBlock = kRowsPerPass * kRowsPerThread;     // 64 rows per block
+
+__global__ void __launch_bounds__(kThreads)
+    perm256_kernel(int layout, int n_shards, int seq, int s_n, int inverse, int64_t rows_outer,
+                   const uint4* __restrict__ src, uint4* __restrict__ dst) {
+  const int lane16 = threadIdx.x & 15;
+  const int sub = threadIdx.x >> 4;
+  const int j0 = blockIdx.x * kRowsPerBlock;
+  for (int64_t o = blockIdx.y; o < rows_outer; o += gridDim.y) {
+    const uint4* s = src + o * (int64_t)seq * 16;
+    uint4* d = dst + o * (int64_t)seq * 16;
+    uint4 v[kRowsPerThread];
+    int to[kRowsPerThread];
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r) {
+      const int j = j0 + r * kRowsPerPass + sub;
+      to[r] = -1;
+      if (j < seq) {
+        const int p = j / s_n;
+        const int pj = (int)pos_of(layout, n_shards, s_n, p, j - p * s_n);
+        const int from = inverse ? j : pj;
+        to[r] = inverse ? pj : j;
+        v[r] = s[(int64_t)from * 16 + lane16];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerThread; ++r)
+      if (to[r] >= 0) d[(int64_t)to[r] * 16 + lane16] = v[r];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_layout_perm(int layout, int64_t seq, int n_shards, int inverse,
                                int64_t rows_outer, int row_bytes, const void* src, void* dst,
                                cudaStream_t stream) {
   const int64_t s_n = seq / n_shards;
+  if (row_bytes == 256) {
+    const int64_t gy = rows_outer < 65535 ? rows_outer : 65535;
+    dim3 grid((unsigned)((seq + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)gy);
+    perm256_kernel<<<grid, kThreads, 0, stream>>>(layout, n_shards, (int)seq, (int)s_n, inverse, rows_outer,
+                                                 static_cast<const uint4*>(src), static_cast<uint4*>(dst));
+    return cudaGetLastError();
+  }
   const bool v16 = (row_bytes % 16) == 0;
   const int vpr = v16 ? row_bytes / 16 : row_bytes / 4;
   const int64_t per_outer = seq * vpr;
