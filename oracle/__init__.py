@@ -34,6 +34,9 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
                             Module 23's (2,4,96,32) example, full and causal, within the
                             page's 1e-5; layout invariance after un-permuting.
 ``ring_partials``           merging them reproduces ``full_attention``.
+``pass_blocks``,            after t exchanges slot p holds the block that started in slot
+``held_blocks``             (p - t) mod N (labelled rows); N exchanges are the identity;
+                            attention over the held block equals ``ring_partials`` entry t.
 ``merge_partials``          splitting the keys into halves and merging reproduces
                             ``full_attention``; -inf parts are ignored.
 ``tile_counts``             brute force over every (q, k) pair of every tile on small
@@ -45,7 +48,7 @@ No function here is "parity unpinned".
 
 from .layouts import CONTIGUOUS, STRIPED, ZIGZAG, LAYOUTS, layout_positions, causal_pair_counts
 from .attention import attention_rows, full_attention, full_attention_rows
-from .ring import ring_sim, ring_partials
+from .ring import ring_sim, ring_partials, pass_blocks, held_blocks
 from .merge import merge_partials
 from .tiles import tile_counts, tile_classes_bruteforce
 
@@ -53,6 +56,6 @@ __all__ = [
     "CONTIGUOUS", "STRIPED", "ZIGZAG", "LAYOUTS",
     "layout_positions", "causal_pair_counts",
     "full_attention", "full_attention_rows", "attention_rows",
-    "ring_sim", "ring_partials", "merge_partials",
+    "ring_sim", "ring_partials", "pass_blocks", "held_blocks", "merge_partials",
     "tile_counts", "tile_classes_bruteforce",
 ]

@@ -135,3 +135,29 @@ def ring_partials(q, k, v, n_shards, positions=None, causal=False, scale=None):
                         o_parts[t, b, h, rows] = np.where(l[:, None] > 0, o / l[:, None], 0.0)
                         lse_parts[t, b, h, rows] = np.where(l > 0, m + np.log(l), -np.inf)
     return o_parts, lse_parts
+
+
+def pass_blocks(x, n_shards):
+    """One exchange of the ring: every device hands the block it holds to the next.
+
+    x: [..., S, d] in layout order (shard p owns rows [p*S/N, (p+1)*S/N)).  Returns a
+    new array in which shard p's rows hold what shard p-1 (mod N) held -- device
+    i -> i+1 (3.6, "Ring Attention"; the Q&A page, "The ring", rotates its block
+    list the same way).
+    """
+    x = np.asarray(x)
+    S = x.shape[-2]
+    if S % n_shards:
+        raise ValueError("seq must be a multiple of n_shards")
+    s_n = S // n_shards
+    blocks = [x[..., p * s_n:(p + 1) * s_n, :] for p in range(n_shards)]
+    received = [blocks[(p - 1) % n_shards] for p in range(n_shards)]
+    return np.concatenate(received, axis=-2)
+
+
+def held_blocks(x, n_shards, step):
+    """What every device holds at ring step ``step``: ``step`` exchanges of ``pass_blocks``."""
+    x = np.asarray(x)
+    for _ in range(step):
+        x = pass_blocks(x, n_shards)
+    return x

@@ -329,3 +329,49 @@ def test_attention_rows_equals_full():
                                    k_positions=pos, causal=True)
     np.testing.assert_allclose(o3, o2, atol=1e-14)
     np.testing.assert_allclose(l3, l2, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# The K/V exchange (what each device holds at each step)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5])
+def test_pass_blocks_closed_form(n):
+    # rows labelled by their starting position: after t exchanges, the rows of
+    # slot p are those that started in slot (p - t) mod N, in their own order
+    s_n, S = 4, 4 * n
+    x = np.arange(2 * S, dtype=np.float64).reshape(1, 2, S, 1).repeat(3, axis=-1)
+    for t in range(2 * n + 1):
+        y = oracle.held_blocks(x, n, t)
+        for p in range(n):
+            src = (p - t) % n
+            np.testing.assert_array_equal(y[..., p * s_n:(p + 1) * s_n, :], x[..., src * s_n:(src + 1) * s_n, :])
+    np.testing.assert_array_equal(oracle.held_blocks(x, n, n), x)
+    if n > 1:  # direction: device i sends to i+1, so slot 1 now holds slot 0's rows
+        np.testing.assert_array_equal(oracle.pass_blocks(x, n)[..., s_n:2 * s_n, :], x[..., :s_n, :])
+
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, ZIGZAG])
+def test_held_blocks_give_ring_partials(layout):
+    # attention of each device's rows over the block it holds at step t, with that
+    # block's positions, is partial t of ring_partials
+    B, Hq, Hkv, S, d, n = 1, 2, 1, 24, 4, 3
+    q, k, v = _rand((B, Hq, S, d), 60), _rand((B, Hkv, S, d), 61), _rand((B, Hkv, S, d), 62)
+    pos = layout_positions(layout, S, n)
+    op, lp = ring_partials(q, k, v, n, positions=pos, causal=True)
+    s_n = S // n
+    for t in range(n):
+        kh, vh = oracle.held_blocks(k, n, t), oracle.held_blocks(v, n, t)
+        ph = oracle.held_blocks(pos.reshape(S, 1), n, t)[:, 0]
+        for p in range(n):
+            rows = slice(p * s_n, (p + 1) * s_n)
+            for h in range(Hq):
+                allowed = ph[rows][None, :] <= pos[rows][:, None]
+                if not allowed.any():
+                    assert np.all(np.isneginf(lp[t, 0, h, rows]))
+                    continue
+                o, l = oracle.attention_rows(q[0, h, rows], kh[0, 0, rows], vh[0, 0, rows],
+                                             q_positions=pos[rows], k_positions=ph[rows], causal=True)
+                ok = np.isfinite(l)
+                np.testing.assert_allclose(o[ok], op[t, 0, h, rows][ok], atol=1e-13)
+                np.testing.assert_allclose(l, lp[t, 0, h, rows], atol=1e-13)
