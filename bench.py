@@ -193,6 +193,21 @@ def run_ours(args, wl):
     lse_n = torch.empty_like(lse_l)
     stream = torch.cuda.current_stream()
     launches_per_step = 6
+    if args.path == "ring":
+        # explicit ring driver: scratch for two receive buffers and the N partials
+        kbuf = torch.empty((2,) + tuple(k.shape), dtype=k.dtype, device=dev)
+        vbuf = torch.empty_like(kbuf)
+        o_parts = torch.empty((N,) + tuple(q.shape), dtype=torch.float32, device=dev)
+        lse_parts = torch.empty((N,) + tuple(lse_l.shape), dtype=torch.float32, device=dev)
+        comm = torch.cuda.Stream(device=dev)
+        launches_per_step = 5 + N + 1   # permutes, one forward launch per ring step, the merge
+
+    def forward(qx, kx, vx):
+        if args.path == "ring":
+            ra.ra_ring_fwd(plan, qx, kx, vx, o=o_l, lse=lse_l, k_buf=kbuf, v_buf=vbuf, o_parts=o_parts,
+                           lse_parts=lse_parts, comm_stream=comm)
+        else:
+            ra.ra_fwd(plan, qx, kx, vx, o=o_l, lse=lse_l)
 
     def step(ev=None):
         if ev is not None:
@@ -202,7 +217,7 @@ def run_ours(args, wl):
         ra.ra_layout_perm(v, layout, N, out=vl)
         if ev is not None:
             ev[1].record(stream)
-        ra.ra_fwd(plan, ql, kl, vl, o=o_l, lse=lse_l)
+        forward(ql, kl, vl)
         if ev is not None:
             ev[2].record(stream)
         ra.ra_layout_perm(o_l, layout, N, inverse=True, out=o_n)
@@ -273,7 +288,7 @@ def run_ours(args, wl):
                 ra.ra_layout_perm(bk, layout, N, out=kl)
                 ra.ra_layout_perm(bv, layout, N, out=vl)
                 in_free[b].record(stream)
-                ra.ra_fwd(plan, ql, kl, vl, o=o_l, lse=lse_l)
+                forward(ql, kl, vl)
                 if i >= 2:
                     stream.wait_event(d2h_done[b])   # step i-2's outputs have left this slot
                 ra.ra_layout_perm(o_l, layout, N, inverse=True, out=bo)
@@ -321,6 +336,11 @@ def run_ours(args, wl):
             "merge": merge_bandwidth(ra, torch, dev, stream),
         }
 
+    ring = None
+    if args.path == "ring":
+        ring = ring_driver_report(ra, torch, plan, N, (ql, kl, vl), (o_l, lse_l), (kbuf, vbuf),
+                                  (o_parts, lse_parts), stream, statistics.mean(fwd_ms), flops)
+
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
@@ -349,6 +369,11 @@ def run_ours(args, wl):
         "algorithmic_flops_per_step": flops,
         "kernels": kernels,
     }
+    if ring is not None:
+        line["ring_driver"] = ring
+        line["config"]["path"] = "ring driver: per-step launches, K/V exchange on a second stream, merge"
+        line["roofline"]["kernel"] = "fwd_bf16_kernel (one launch per ring step) + merge_kernel"
+        line["roofline"]["traffic"] = None
     if kernels is not None:
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         for kv in kernels.values():
@@ -400,6 +425,56 @@ def measured_traffic(workload):
         return None
 
 
+def ring_driver_report(ra, torch, plan, N, qkv, out, bufs, parts, stream, driver_ms, flops):
+    """Where the explicit ring driver's time goes: its pieces timed one by one.
+
+    steps_only: the N per-step launches back to back (K/V read from one buffer;
+    the data does not change the work).  rotations_only: the N-1 exchanges back to
+    back.  merge_only: the final merge.  With the exchange hidden behind compute the
+    driver takes about steps_only + merge_only.
+    """
+    ql, kl, vl = qkv
+    o_l, lse_l = out
+    kbuf, vbuf = bufs
+    o_parts, lse_parts = parts
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    def steps():
+        for t in range(N):
+            ra.ra_fwd_step(plan, t, ql, kl, vl, o_part=o_parts[t], lse_part=lse_parts[t])
+
+    def rotations():
+        src_k, src_v = kl, vl
+        for t in range(N - 1):
+            ra.ra_ring_rotate(plan, src_k, src_v, kbuf[t % 2], vbuf[t % 2])
+            src_k, src_v = kbuf[t % 2], vbuf[t % 2]
+
+    def merge():
+        ra.ra_merge_partials(o_parts, lse_parts, o=o_l, lse=lse_l)
+
+    steps_ms, rot_ms, merge_ms = timed(steps), timed(rotations), timed(merge)
+    fused_ms = timed(lambda: ra.ra_fwd(plan, ql, kl, vl, o=o_l, lse=lse_l))
+    ra.ra_sync_status(plan)
+    rot_bytes = 2 * (N - 1) * 2 * kl.numel() * kl.element_size()   # K and V, read + write
+    serial = steps_ms + rot_ms + merge_ms
+    return {
+        "driver_ms": driver_ms, "driver_TFLOP/s": flops / (driver_ms * 1e-3) / 1e12,
+        "steps_only_ms": steps_ms, "rotations_only_ms": rot_ms, "merge_only_ms": merge_ms,
+        "rotation_GB/s": rot_bytes / rot_ms / 1e6 if rot_ms > 0 else None,
+        "serial_sum_ms": serial,
+        "rotation_hidden_frac": (serial - driver_ms) / rot_ms if rot_ms > 0 else None,
+        "fused_ra_fwd_ms": fused_ms,
+    }
+
+
 def merge_bandwidth(ra, torch, dev, stream, n_parts=8, rows=1 << 20, d=128, reps=5):
     """ra_merge_partials on 8 synthetic float32 parts of 1M rows x 128 -> bf16 (HBM-bound)."""
     g = torch.Generator(device=dev).manual_seed(77)
@@ -433,6 +508,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip the permute/merge bandwidth lines")
+    ap.add_argument("--path", default="fused", choices=["fused", "ring"],
+                    help="fused: one ra_fwd launch per step; ring: the explicit ring driver "
+                         "(per-step launches, K/V exchange on a second stream, merge)")
     args = ap.parse_args()
     from context_ring_attention_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]

@@ -1,8 +1,9 @@
 """GB300 ring-attention forward: Python binding of libra.so (include/ra.h).
 
-The functions keep the C names (``ra_plan``, ``ra_fwd``, ``ra_merge_partials``,
-``ra_layout_perm``, ``ra_layout_index``, ``ra_plan_tile_counts``,
-``ra_sync_status``, ``ra_last_error``).  This module only marshals arguments:
+The functions keep the C names (``ra_plan``, ``ra_fwd``, ``ra_fwd_step``,
+``ra_ring_rotate``, ``ra_ring_fwd``, ``ra_merge_partials``, ``ra_layout_perm``,
+``ra_layout_index``, ``ra_plan_tile_counts``, ``ra_sync_status``,
+``ra_last_error``, ``ra_fwd_static``).  This module only marshals arguments:
 PyTorch supplies device memory and the current stream, every step of the
 computation runs in the library's CUDA kernels, and there is no fallback -- if
 libra.so is missing or cannot be loaded, every call raises.
@@ -20,6 +21,7 @@ __all__ = [
     "RaError", "Plan", "LAYOUTS",
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
+    "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -28,7 +30,8 @@ DTYPES = {"f32": 0, "bf16": 1}
 _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
            4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
-            "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static")
+            "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
+            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -73,6 +76,9 @@ def load_library():
         "ra_sync_status": ([P, VP], I32),
         "ra_last_error": ([], ctypes.c_char_p),
         "ra_fwd_static": ([ctypes.POINTER(_Problem), VP, VP, VP, VP, VP, VP], I32),
+        "ra_fwd_step": ([P, I32, VP, VP, VP, VP, VP, VP], I32),
+        "ra_ring_rotate": ([P, VP, VP, VP, VP, VP], I32),
+        "ra_ring_fwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -159,16 +165,25 @@ def ra_plan_tile_counts(plan):
     return full, part, skip
 
 
+def _check_qkv(plan, **tensors):
+    """Shape/dtype/contiguity of q ([B, Hq, S, d]) and K/V-like ([B, Hkv, S, d]) arguments."""
+    import torch
+    pb = plan.problem
+    B, S, d = pb["batch"], pb["seq"], pb["head_dim"]
+    dt = torch.bfloat16 if pb["dtype"] == 1 else torch.float32
+    for name, t in tensors.items():
+        heads = pb["heads_q"] if name == "q" else pb["heads_kv"]
+        if tuple(t.shape) != (B, heads, S, d) or t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {(B, heads, S, d)}")
+
+
 def ra_fwd(plan, q, k, v, o=None, lse=None, partials=False, o_parts=None, lse_parts=None,
            stream=None):
     """Ring-attention forward.  Fused: returns (O, LSE).  partials=True: (O_parts, LSE_parts)."""
     import torch
     pb = plan.problem
     B, Hq, S, d, N = pb["batch"], pb["heads_q"], pb["seq"], pb["head_dim"], pb["n_shards"]
-    dt = torch.bfloat16 if pb["dtype"] == 1 else torch.float32
-    for name, t, heads in (("q", q, Hq), ("k", k, pb["heads_kv"]), ("v", v, pb["heads_kv"])):
-        if tuple(t.shape) != (B, heads, S, d) or t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
-            raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {(B, heads, S, d)}")
+    _check_qkv(plan, q=q, k=k, v=v)
     lib = load_library()
     if partials:
         if o_parts is None:
@@ -256,4 +271,70 @@ def ra_fwd_static(batch, seq, heads_q, heads_kv, n_shards, layout, causal, q, k,
                     int(bool(causal)), 1, float(scale or 0.0))
     _check(load_library().ra_fwd_static(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                         _stream(stream)))
+    return o, lse
+
+
+def ra_fwd_step(plan, step, q, k_blk, v_blk, o_part=None, lse_part=None, stream=None):
+    """One ring step for every shard over the blocks the shards hold -> (O_t, LSE_t) in float32.
+
+    ``k_blk``/``v_blk`` hold, in the rows of shard p, the block shard p holds at this
+    step (K/V themselves at step 0; ``ra_ring_rotate`` passes them on).
+    """
+    import torch
+    pb = plan.problem
+    B, Hq, S, d = pb["batch"], pb["heads_q"], pb["seq"], pb["head_dim"]
+    _check_qkv(plan, q=q, k_blk=k_blk, v_blk=v_blk)
+    if o_part is None:
+        o_part = torch.empty((B, Hq, S, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _check(load_library().ra_fwd_step(plan.handle, int(step), _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(o_part),
+                                      _ptr(lse_part), _stream(stream)))
+    return o_part, lse_part
+
+
+def ra_ring_rotate(plan, k_src, v_src, k_dst=None, v_dst=None, stream=None):
+    """Pass every shard's K/V block on to the next shard -> (k_dst, v_dst)."""
+    import torch
+    _check_qkv(plan, k_src=k_src, v_src=v_src)
+    if k_dst is None:
+        k_dst = torch.empty_like(k_src)
+    if v_dst is None:
+        v_dst = torch.empty_like(v_src)
+    _check_qkv(plan, k_dst=k_dst, v_dst=v_dst)
+    _check(load_library().ra_ring_rotate(plan.handle, _ptr(k_src), _ptr(v_src), _ptr(k_dst), _ptr(v_dst),
+                                         _stream(stream)))
+    return k_dst, v_dst
+
+
+def ra_ring_fwd(plan, q, k, v, o=None, lse=None, k_buf=None, v_buf=None, o_parts=None, lse_parts=None,
+                stream=None, comm_stream=None):
+    """Explicit ring driver: N per-step launches, K/V passed on on ``comm_stream``, then a merge.
+
+    Returns (O, LSE).  Scratch (two receive buffers for K and V, the N float32
+    partials) is allocated here unless passed in; ``comm_stream`` defaults to a
+    new stream (pass the compute stream itself to run without overlap).
+    """
+    import torch
+    pb = plan.problem
+    B, Hq, S, d, N = pb["batch"], pb["heads_q"], pb["seq"], pb["head_dim"], pb["n_shards"]
+    _check_qkv(plan, q=q, k=k, v=v)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if N > 1:
+        if k_buf is None:
+            k_buf = torch.empty((2,) + tuple(k.shape), dtype=k.dtype, device=k.device)
+        if v_buf is None:
+            v_buf = torch.empty((2,) + tuple(v.shape), dtype=v.dtype, device=v.device)
+    if o_parts is None:
+        o_parts = torch.empty((N, B, Hq, S, d), dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((N, B, Hq, S), dtype=torch.float32, device=q.device)
+    if comm_stream is None:
+        comm_stream = torch.cuda.Stream(device=q.device)
+    _check(load_library().ra_ring_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_buf),
+                                      _ptr(v_buf), _ptr(o_parts), _ptr(lse_parts), _stream(stream),
+                                      _stream(comm_stream)))
     return o, lse

@@ -135,7 +135,7 @@ struct Walk {
 };
 
 __device__ __forceinline__ void walk_to_next_step(Walk& w, const FwdParams& P, int p, int64_t maxq) {
-  for (++w.t; w.t < P.n_shards; ++w.t) {
+  for (++w.t; w.t < P.step_hi; ++w.t) {
     w.r = (p - w.t + P.n_shards) % P.n_shards;
     w.nt = visit_tiles(P.layout, P.n_shards, P.s_n, P.causal, w.r, maxq);
     if (w.nt > 0) {
@@ -145,7 +145,7 @@ __device__ __forceinline__ void walk_to_next_step(Walk& w, const FwdParams& P, i
   }
 }
 __device__ __forceinline__ void walk_begin(Walk& w, const FwdParams& P, int p, int64_t maxq) {
-  w.t = -1;
+  w.t = P.step_lo - 1;
   w.kt = 0;
   w.nt = 0;
   walk_to_next_step(w, P, p, maxq);
@@ -155,11 +155,15 @@ __device__ __forceinline__ void walk_advance(Walk& w, const FwdParams& P, int p,
 }
 
 // ------------------------------------------------------------- work items --
-// Items are handed out dynamically: the producer warp takes the next index of the
-// (longest-first, key/value-head-grouped) list from a global counter and passes it
-// to the other roles through a small ring in shared memory.  The items in flight
-// across the GPU are then always neighbours in the list, so the CTAs running
-// together share K/V tiles in L2, and the grid ends evenly.
+// The producer warp decides which item comes next and passes its index to the
+// other roles through a small ring in shared memory.  Two schedules:
+//  - dynamic: the next index of the (longest-first, key/value-head-grouped) list
+//    from a global counter, so the items in flight are always neighbours in the
+//    list and the grid ends evenly;
+//  - round-synchronised (large problems): round u gives CTA b item u*grid + b and
+//    begins only when every CTA has issued the previous round's loads.  The CTAs
+//    of a round then walk the same K/V at the same pace instead of drifting apart
+//    over long items, and the K/V they stream stays within L2.
 
 // Consumer side: index of this role's u-th item, or -1 at the end / on abort.
 __device__ __forceinline__ int next_item(const Ctl& c, volatile int32_t* slots, uint32_t u, int lane) {
@@ -180,6 +184,32 @@ struct ProducerState {
   uint32_t q_issued;
 };
 
+// Producer-side grid barrier for round-synchronised schedules: wait (bounded, like
+// every wait here) until the shared counter reaches `need`.
+__device__ __forceinline__ bool barrier_wait(const Ctl& c, const uint32_t* counter, uint32_t need, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    const volatile uint32_t* ctr = counter;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 0; *ctr < need; ++it) {
+      __nanosleep(128);
+      if ((it & 63u) == 63u) {
+        if (*c.abort) {
+          ok = 0;
+          break;
+        }
+        if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
+          *c.abort = 1u;
+          atomicOr(c.status, kStatusTimeoutProducer);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
                              const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              ProducerState& st) {
@@ -192,10 +222,19 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
     const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kItemEmpty + (int)slot), (use & 1u) ^ 1u, kStatusTimeoutProducer)))
       break;
-    int idx = 0;
-    if (lane == 0) idx = (int)atomicAdd(P.item_counter, 1u);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
-    if (idx >= P.n_items) idx = -1;
+    int idx;
+    if (P.round_sync) {
+      // Round u: item u*grid + b, once every CTA has issued the loads of round u-1
+      // (all earlier rounds are full: only the last one can be short).
+      idx = (int)(u * gridDim.x + blockIdx.x);
+      if (idx >= P.n_items) idx = -1;
+      if (idx >= 0 && u > 0 && !barrier_wait(c, P.item_counter, u * gridDim.x, lane)) idx = -1;
+    } else {
+      idx = 0;
+      if (lane == 0) idx = (int)atomicAdd(P.item_counter, 1u);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (idx >= P.n_items) idx = -1;
+    }
     if (lane == 0) slots[slot] = idx;
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
@@ -219,8 +258,9 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
     Walk w;
     walk_begin(w, P, it.shard, it.maxq);
     bool ok = true;
-    while (ok && w.t < P.n_shards) {
-      const int32_t y = (int32_t)(kv_base + (int64_t)w.r * P.s_n + (int64_t)w.kt * kTileRows);
+    while (ok && w.t < P.step_hi) {
+      const int slot = P.kv_rotated ? it.shard : w.r;  // where the block of step t sits
+      const int32_t y = (int32_t)(kv_base + (int64_t)slot * P.s_n + (int64_t)w.kt * kTileRows);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // K tile, then V tile
         const uint32_t s = kv_it % kStages, use = kv_it / kStages;
@@ -238,6 +278,10 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
       walk_advance(w, P, it.shard, it.maxq);
     }
     if (!ok) break;
+    if (P.round_sync) {
+      if (lane == 0) atomicAdd(P.item_counter, 1u);  // this CTA has issued its round
+      __syncwarp();
+    }
   }
 }
 
@@ -288,7 +332,7 @@ __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volati
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kQFull), u & 1u, kStatusTimeoutMma))) return;
     Walk cur;
     walk_begin(cur, P, it.shard, it.maxq);
-    if (cur.t >= P.n_shards) {
+    if (cur.t >= P.step_hi) {
       ptx::mma_commit_warp(c.bar(kQEmpty));
       continue;
     }
@@ -306,7 +350,7 @@ __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volati
     for (;;) {
       Walk nxt = cur;
       walk_advance(nxt, P, it.shard, it.maxq);
-      const bool has_next = nxt.t < P.n_shards;
+      const bool has_next = nxt.t < P.step_hi;
       const bool seg_first = partials ? (cur.kt == 0) : first_tile;
       const bool seg_last = partials ? (!has_next || nxt.t != cur.t) : !has_next;
       const uint32_t vs = kv_it % kStages;
@@ -415,19 +459,20 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
     const int64_t my_pos = pos_of(P.layout, N, P.s_n, p, valid ? i : P.s_n - 1);
     const int64_t out_row = (int64_t)bh * P.seq + (int64_t)p * P.s_n + i;
     int last_t = -1;
-    for (int t = 0; t < N; ++t)
+    for (int t = P.step_lo; t < P.step_hi; ++t)
       if (visit_tiles(P.layout, N, P.s_n, P.causal, (p - t + N) % N, it.maxq) > 0) last_t = t;
 
     float m = -INFINITY, l = 0.f;
     bool open = false;
-    for (int t = 0; t < N; ++t) {
+    for (int t = P.step_lo; t < P.step_hi; ++t) {
       const int r = (p - t + N) % N;
       const int nt = visit_tiles(P.layout, N, P.s_n, P.causal, r, it.maxq);
+      const int part = t - P.step_lo;  // index of this step's partial
       if (nt == 0) {
         if (partials && valid) {  // nothing of this block is causal for the tile
-          float4* dst = reinterpret_cast<float4*>(P.o_parts + ((int64_t)t * rows_all + out_row) * 128);
+          float4* dst = reinterpret_cast<float4*>(P.o_parts + ((int64_t)part * rows_all + out_row) * 128);
           for (int q = 0; q < 32; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-          P.lse_parts[(int64_t)t * rows_all + out_row] = -INFINITY;
+          P.lse_parts[(int64_t)part * rows_all + out_row] = -INFINITY;
         }
         continue;
       }
@@ -526,7 +571,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
           ++oj;
           if (!__all_sync(0xffffffffu, ok)) return;
           ptx::tc_fence_after();
-          store_segment(P, tO, m, l, valid, out_row, t);
+          store_segment(P, tO, m, l, valid, out_row, part);
           ptx::tc_fence_before();
           m = -INFINITY;
           l = 0.f;
@@ -681,8 +726,25 @@ cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, 
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
-  e = cudaGetLastError();
+  if (prm.round_sync) {
+    // The rounds wait on each other: a cooperative launch guarantees that every CTA
+    // is resident at once (it fails instead of starting otherwise).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute coop[1];
+    coop[0].id = cudaLaunchAttributeCooperative;
+    coop[0].val.cooperative = 1;
+    cfg.attrs = coop;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fwd_bf16_kernel, tq, tk, tv, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  } else {
+    fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) *why = "tensor-core forward launch failed";
   return e;
 }

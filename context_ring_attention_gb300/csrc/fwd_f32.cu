@@ -54,12 +54,13 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
   for (int x = 0; x < kMaxD / 32; ++x) acc[x] = 0.f;
 
-  for (int t = 0; t < N; ++t) {
+  for (int t = P.step_lo; t < P.step_hi; ++t) {
     const int r = (p - t + N) % N;
     // Keys of shard r with position <= my_pos are rows 0..J (positions rise with the row).
     const int64_t nkeys = P.causal ? last_le(P.layout, N, P.s_n, r, my_pos) + 1 : P.s_n;
-    const float* kb = k + (kv_base + (int64_t)r * P.s_n) * d;
-    const float* vb = v + (kv_base + (int64_t)r * P.s_n) * d;
+    const int slot = P.kv_rotated ? p : r;  // where the block of step t sits
+    const float* kb = k + (kv_base + (int64_t)slot * P.s_n) * d;
+    const float* vb = v + (kv_base + (int64_t)slot * P.s_n) * d;
     for (int64_t j0 = 0; j0 < nkeys; j0 += 32) {
       const int64_t j = j0 + lane;
       float s = -INFINITY;
@@ -88,7 +89,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       m = m_new;
     }
     if (partials) {  // this step's block alone, then start afresh
-      float* dst = P.o_parts + ((int64_t)t * rows_all + grow) * d;
+      float* dst = P.o_parts + ((int64_t)(t - P.step_lo) * rows_all + grow) * d;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
       for (int x = 0; x < kMaxD / 32; ++x) {
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         if (col < d) dst[col] = acc[x] * inv;
         acc[x] = 0.f;
       }
-      if (lane == 0) P.lse_parts[(int64_t)t * rows_all + grow] = l > 0.f ? m + logf(l) : -INFINITY;
+      if (lane == 0) P.lse_parts[(int64_t)(t - P.step_lo) * rows_all + grow] = l > 0.f ? m + logf(l) : -INFINITY;
       m = -INFINITY;
       l = 0.f;
     }

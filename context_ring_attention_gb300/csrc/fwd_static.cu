@@ -59,14 +59,16 @@ ra_status check_problem(const ra_problem* p) {
   if (!(p->scale >= 0.f) || std::isinf(p->scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite and >= 0");
   if (p->dtype != RA_DTYPE_BF16 || p->head_dim != 128)
     return fail(RA_ERR_UNSUPPORTED, "only bf16 with head_dim 128 is supported");
+  if (p->n_shards > INT16_MAX) return fail(RA_ERR_UNSUPPORTED, "n_shards above 32767");
   if (p->seq > INT32_MAX || p->batch > INT32_MAX / p->heads_q || p->batch * (int64_t)p->heads_q * p->seq > INT32_MAX)
     return fail(RA_ERR_UNSUPPORTED, "more than 2^31-1 rows");
   return RA_OK;
 }
 
 // The planner's work list (same items, same schedule order), written into
-// the static host buffer.  Returns the item count, or -1 when it would not fit.
-int64_t build_items(const ra_problem& pb) {
+// the static host buffer.  Returns the item count, or -1 when it would not fit;
+// *max_cost receives the longest item's key-tile count.
+int64_t build_items(const ra_problem& pb, int64_t* max_cost_out) {
   const int N = pb.n_shards;
   const int64_t s_n = pb.seq / N;
   const int n_qt = (int)((s_n + ra::kTileRows - 1) / ra::kTileRows);
@@ -103,6 +105,7 @@ int64_t build_items(const ra_problem& pb) {
         }
   int64_t max_cost = 1;
   for (int64_t i = 0; i < n; ++i) max_cost = std::max<int64_t>(max_cost, g_host_items[i].w.cost);
+  *max_cost_out = max_cost;
   const int64_t width = ra::schedule_bucket_width(max_cost);
   const int G = pb.heads_q / pb.heads_kv;
   std::sort(g_host_items, g_host_items + n, [&](const Keyed& a, const Keyed& b) {
@@ -124,7 +127,8 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
     if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u)) return fail(RA_ERR_INVALID_ARG, "pointer not 16-byte aligned");
 
   std::lock_guard<std::mutex> lock(g_mutex);
-  const int64_t n_items = build_items(*prob);
+  int64_t max_cost = 0;
+  const int64_t n_items = build_items(*prob, &max_cost);
   if (n_items < 0) return fail(RA_ERR_UNSUPPORTED, "work list exceeds the static maximum of 131072 items");
 
   int dev = -1;
@@ -165,8 +169,8 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   prm.group = prob->heads_q / prob->heads_kv;
   prm.head_dim = prob->head_dim;
   prm.n_shards = prob->n_shards;
-  prm.layout = prob->layout;
-  prm.causal = prob->causal;
+  prm.layout = (int16_t)prob->layout;
+  prm.causal = (int16_t)prob->causal;
   prm.seq = prob->seq;
   prm.s_n = prob->seq / prob->n_shards;
   prm.n_items = (int32_t)n_items;
@@ -179,10 +183,19 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   prm.lse_parts = nullptr;
   prm.status = reinterpret_cast<uint32_t*>(base);
   prm.item_counter = reinterpret_cast<uint32_t*>(base) + 1;
+  prm.step_lo = 0;
+  prm.step_hi = (int16_t)prob->n_shards;
+  prm.kv_rotated = 0;
+  prm.round_sync = ra::use_round_sync(prob->seq, prob->head_dim, max_cost) ? 1 : 0;
   if (n_items == 0) return RA_OK;
   const int grid = (int)std::min<int64_t>(n_items, g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 148);
   const char* why = "";
   e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {  // not every CTA resident: dynamic schedule
+    cudaGetLastError();
+    prm.round_sync = 0;
+    e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
+  }
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, why);
   ra::set_last_error("");
   return RA_OK;

@@ -7,7 +7,8 @@
 // visits over the N ring steps.  Items are ordered longest first so the
 // persistent grid ends evenly under a causal mask, whose per-shard work is
 // uneven for contiguous shards (Module 23, "The Causal Imbalance -- and the
-// Striped Fix").
+// Striped Fix").  For per-step launches (ra_fwd_step, ra_ring_fwd) the plan also
+// holds one list per ring step, ordered by that step's cost alone.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -24,11 +25,16 @@ struct ra_plan_s {
   ra_problem prob;
   int64_t s_n;
   int n_qtiles, n_ktiles;
-  std::vector<ra::WorkItem> items;
+  std::vector<ra::WorkItem> items;       // whole forward: all N steps per item
+  std::vector<ra::WorkItem> step_items;  // per-step lists, concatenated
+  std::vector<int64_t> step_off;         // list of step t is [step_off[t], step_off[t+1])
   std::vector<int64_t> full, partial, skip;
   int device = -1;
   ra::WorkItem* d_items = nullptr;
+  ra::WorkItem* d_step_items = nullptr;
   uint32_t* d_status = nullptr;
+  cudaEvent_t ev_entry = nullptr, ev_rot = nullptr, ev_step = nullptr;  // ra_ring_fwd ordering
+  bool round_sync = false;  // forward kernel schedule (ra::use_round_sync)
   int sm_count = 0;
 };
 
@@ -59,6 +65,7 @@ ra_status check_layout(int32_t layout, int64_t seq, int32_t n) {
   if (layout == RA_LAYOUT_ZIGZAG && seq % (2 * (int64_t)n))
     return fail(RA_ERR_INVALID_ARG, "zigzag needs seq %lld to be a multiple of 2*n_shards", (long long)seq);
   if (seq > INT32_MAX) return fail(RA_ERR_UNSUPPORTED, "seq above 2^31-1");
+  if (n > INT16_MAX) return fail(RA_ERR_UNSUPPORTED, "n_shards above 32767");
   return RA_OK;
 }
 
@@ -86,6 +93,26 @@ ra_status validate(const ra_problem* p) {
 int64_t last_row_pos(const ra_problem& pb, int64_t s_n, int p, int64_t row_start) {
   const int64_t last = std::min<int64_t>(row_start + ra::kTileRows, s_n) - 1;
   return ra::pos_of(pb.layout, pb.n_shards, s_n, p, last);
+}
+
+struct Keyed {
+  ra::WorkItem w;
+  int64_t order;  // creation order, the last tie-break
+};
+
+// Items in schedule order (ra::schedule_before on their current cost).
+std::vector<ra::WorkItem> schedule(const std::vector<Keyed>& list, int heads_q, int group) {
+  int64_t max_cost = 1;
+  for (const Keyed& k : list) max_cost = std::max<int64_t>(max_cost, k.w.cost);
+  const int64_t width = ra::schedule_bucket_width(max_cost);
+  std::vector<ra::ScheduleKey> keys(list.size());
+  for (size_t n = 0; n < list.size(); ++n) keys[n] = ra::schedule_key(list[n].w, heads_q, group, width, list[n].order);
+  std::vector<size_t> idx(list.size());
+  for (size_t n = 0; n < idx.size(); ++n) idx[n] = n;
+  std::sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return ra::schedule_before(keys[a], keys[b]); });
+  std::vector<ra::WorkItem> out(list.size());
+  for (size_t n = 0; n < list.size(); ++n) out[n] = list[idx[n]].w;
+  return out;
 }
 
 void build_schedule(ra_plan_s* pl) {
@@ -128,10 +155,6 @@ void build_schedule(ra_plan_s* pl) {
 
   const int G = pb.heads_q / pb.heads_kv;
   const bool head_pairs = (G % 2) == 0;
-  struct Keyed {
-    ra::WorkItem w;
-    int64_t order;
-  };
   std::vector<Keyed> list;
   int64_t seqno = 0;
   for (int p = 0; p < N; ++p) {
@@ -163,17 +186,24 @@ void build_schedule(ra_plan_s* pl) {
       }
     }
   }
-  int64_t max_cost = 1;
+  pl->items = schedule(list, pb.heads_q, G);
+  int64_t max_cost = 0;
   for (const Keyed& k : list) max_cost = std::max<int64_t>(max_cost, k.w.cost);
-  const int64_t width = ra::schedule_bucket_width(max_cost);
-  std::vector<ra::ScheduleKey> keys(list.size());
-  for (size_t n = 0; n < list.size(); ++n)
-    keys[n] = ra::schedule_key(list[n].w, pb.heads_q, G, width, list[n].order);
-  std::vector<size_t> idx(list.size());
-  for (size_t n = 0; n < idx.size(); ++n) idx[n] = n;
-  std::sort(idx.begin(), idx.end(), [&](size_t a, size_t b) { return ra::schedule_before(keys[a], keys[b]); });
-  pl->items.resize(list.size());
-  for (size_t n = 0; n < list.size(); ++n) pl->items[n] = list[idx[n]].w;
+  pl->round_sync = ra::use_round_sync(pb.seq, pb.head_dim, max_cost);
+
+  // One list per ring step: the same items, costed by that step's key tiles alone.
+  // Items with no causal key in the step stay in the list (they write the empty
+  // partial: O_t = 0, LSE_t = -inf).
+  pl->step_items.clear();
+  pl->step_off.assign(1, 0);
+  for (int t = 0; t < N; ++t) {
+    std::vector<Keyed> step = list;
+    for (Keyed& k : step)
+      k.w.cost = ra::visit_tiles(pb.layout, N, s_n, pb.causal, (k.w.shard - t + N) % N, k.w.maxq);
+    const std::vector<ra::WorkItem> ordered = schedule(step, pb.heads_q, G);
+    pl->step_items.insert(pl->step_items.end(), ordered.begin(), ordered.end());
+    pl->step_off.push_back((int64_t)pl->step_items.size());
+  }
 }
 
 ra_status upload(ra_plan_s* pl) {
@@ -199,8 +229,109 @@ ra_status upload(ra_plan_s* pl) {
       e = cudaMemcpy(pl->d_items, pl->items.data(), pl->items.size() * sizeof(ra::WorkItem),
                      cudaMemcpyHostToDevice);
   }
+  if (e == cudaSuccess && !pl->step_items.empty()) {
+    e = cudaMalloc(&pl->d_step_items, pl->step_items.size() * sizeof(ra::WorkItem));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(pl->d_step_items, pl->step_items.data(), pl->step_items.size() * sizeof(ra::WorkItem),
+                     cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_entry, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_rot, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_step, cudaEventDisableTiming);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "plan upload failed: %s", cudaGetErrorString(e));
   return RA_OK;
+}
+
+
+// Kernel parameters common to every forward launch of a plan: the whole ring, K/V
+// read in place; callers set items, outputs and, for per-step launches, the range.
+ra::FwdParams fwd_params(const ra_plan_s* plan) {
+  const ra_problem& pb = plan->prob;
+  ra::FwdParams prm{};
+  prm.batch = (int32_t)pb.batch;
+  prm.heads_q = pb.heads_q;
+  prm.heads_kv = pb.heads_kv;
+  prm.group = pb.heads_q / pb.heads_kv;
+  prm.head_dim = pb.head_dim;
+  prm.n_shards = pb.n_shards;
+  prm.layout = (int16_t)pb.layout;
+  prm.causal = (int16_t)pb.causal;
+  prm.seq = pb.seq;
+  prm.s_n = plan->s_n;
+  prm.scale = pb.scale;
+  prm.scale_log2 = pb.scale * 1.4426950408889634f;
+  prm.status = plan->d_status;
+  prm.item_counter = plan->d_status + 1;
+  prm.step_lo = 0;
+  prm.step_hi = (int16_t)pb.n_shards;
+  prm.kv_rotated = 0;
+  prm.round_sync = plan->round_sync ? 1 : 0;
+  return prm;
+}
+
+// Launch the plan's forward kernel (tensor-core for bf16, SIMT for f32) on stream.
+ra_status launch(const ra_plan_s* plan, const ra::FwdParams& prm, const void* q, const void* k,
+                 const void* v, cudaStream_t st) {
+  cudaError_t e;
+  if (plan->prob.dtype == RA_DTYPE_BF16) {
+    if (prm.n_items == 0) return ok();
+    const int grid = std::min(prm.n_items, plan->sm_count > 0 ? plan->sm_count : 148);
+    const char* why = "";
+    // The kernel hands out work items from a counter that starts at zero.
+    e = cudaMemsetAsync(prm.item_counter, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
+    e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {
+      // Not every CTA can be resident (the GPU is shared): the dynamic schedule
+      // needs no co-residency and computes the same result.
+      cudaGetLastError();
+      ra::FwdParams dyn = prm;
+      dyn.round_sync = 0;
+      e = ra::launch_fwd_bf16(dyn, q, k, v, grid, st, &why);
+    }
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
+  } else {
+    e = ra::launch_fwd_f32(prm, static_cast<const float*>(q), static_cast<const float*>(k),
+                           static_cast<const float*>(v), st);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "f32 forward launch failed: %s", cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+ra_status check_device(const ra_plan_s* plan) {
+  if (plan->device < 0) return fail(RA_ERR_NO_DEVICE, "plan was built without a CUDA device");
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
+    return fail(RA_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", cur, plan->device);
+  return RA_OK;
+}
+
+size_t elem_bytes(const ra_problem& pb) { return pb.dtype == RA_DTYPE_BF16 ? 2 : 4; }
+
+bool overlap(const void* a, const void* b, size_t bytes) {
+  const char* x = static_cast<const char*>(a);
+  const char* y = static_cast<const char*>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+// The exchange: dst slot (p + 1) mod N <- src slot p for every [S, d] matrix of a
+// [B, Hkv, S, d] tensor.  Two strided copy-engine transfers: slots 0..N-2 move up
+// by one shard, slot N-1 wraps to slot 0.
+cudaError_t rotate_one(const ra_plan_s* plan, const void* src, void* dst, cudaStream_t st) {
+  const ra_problem& pb = plan->prob;
+  const size_t row = (size_t)pb.head_dim * elem_bytes(pb);
+  const size_t pitch = (size_t)pb.seq * row;
+  const size_t shard = (size_t)plan->s_n * row;
+  const size_t height = (size_t)pb.batch * pb.heads_kv;
+  const int N = pb.n_shards;
+  const char* s = static_cast<const char*>(src);
+  char* d = static_cast<char*>(dst);
+  if (N == 1) return cudaMemcpyAsync(d, s, pitch * height, cudaMemcpyDeviceToDevice, st);
+  cudaError_t e = cudaMemcpy2DAsync(d + shard, pitch, s, pitch, (size_t)(N - 1) * shard, height,
+                                    cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpy2DAsync(d, pitch, s + (size_t)(N - 1) * shard, pitch, shard, height,
+                           cudaMemcpyDeviceToDevice, st);
 }
 
 }  // namespace
@@ -236,7 +367,11 @@ ra_status ra_plan_destroy(ra_plan_t plan) {
     cudaGetDevice(&cur);
     if (cur != plan->device) cudaSetDevice(plan->device);
     cudaFree(plan->d_items);
+    cudaFree(plan->d_step_items);
     cudaFree(plan->d_status);
+    if (plan->ev_entry) cudaEventDestroy(plan->ev_entry);
+    if (plan->ev_rot) cudaEventDestroy(plan->ev_rot);
+    if (plan->ev_step) cudaEventDestroy(plan->ev_step);
     if (cur >= 0 && cur != plan->device) cudaSetDevice(cur);
   }
   delete plan;
@@ -255,7 +390,6 @@ ra_status ra_plan_tile_counts(ra_plan_t plan, int64_t* full, int64_t* partial, i
 ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, void* o, float* lse,
                  float* o_parts, float* lse_parts, void* stream) {
   if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
-  const ra_problem& pb = plan->prob;
   if (q == nullptr || k == nullptr || v == nullptr) return fail(RA_ERR_INVALID_ARG, "null q/k/v");
   const bool partials = o_parts != nullptr || lse_parts != nullptr;
   if (partials) {
@@ -269,50 +403,16 @@ ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, vo
   const void* ptrs[] = {q, k, v, o, lse, o_parts, lse_parts};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
-  if (plan->device < 0) return fail(RA_ERR_NO_DEVICE, "plan was built without a CUDA device");
-  int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
-    return fail(RA_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", cur, plan->device);
-
-  ra::FwdParams prm{};
-  prm.batch = (int32_t)pb.batch;
-  prm.heads_q = pb.heads_q;
-  prm.heads_kv = pb.heads_kv;
-  prm.group = pb.heads_q / pb.heads_kv;
-  prm.head_dim = pb.head_dim;
-  prm.n_shards = pb.n_shards;
-  prm.layout = pb.layout;
-  prm.causal = pb.causal;
-  prm.seq = pb.seq;
-  prm.s_n = plan->s_n;
-  prm.n_items = (int32_t)plan->items.size();
-  prm.scale = pb.scale;
-  prm.scale_log2 = pb.scale * 1.4426950408889634f;
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  ra::FwdParams prm = fwd_params(plan);
   prm.items = plan->d_items;
+  prm.n_items = (int32_t)plan->items.size();
   prm.o = o;
   prm.lse = lse;
   prm.o_parts = o_parts;
   prm.lse_parts = lse_parts;
-  prm.status = plan->d_status;
-  prm.item_counter = plan->d_status + 1;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-
-  cudaError_t e;
-  if (pb.dtype == RA_DTYPE_BF16) {
-    if (prm.n_items == 0) return ok();
-    const int grid = std::min(prm.n_items, plan->sm_count > 0 ? plan->sm_count : 148);
-    const char* why = "";
-    // The kernel hands out work items from a counter that starts at zero.
-    e = cudaMemsetAsync(prm.item_counter, 0, sizeof(uint32_t), st);
-    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
-    e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
-    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
-  } else {
-    e = ra::launch_fwd_f32(prm, static_cast<const float*>(q), static_cast<const float*>(k),
-                           static_cast<const float*>(v), st);
-    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "f32 forward launch failed: %s", cudaGetErrorString(e));
-  }
-  return ok();
+  return launch(plan, prm, q, k, v, static_cast<cudaStream_t>(stream));
 }
 
 ra_status ra_merge_partials(int32_t n_parts, int64_t rows, int32_t d, const float* o_parts,
@@ -357,6 +457,100 @@ ra_status ra_layout_index(int32_t layout, int64_t seq, int32_t n_shards, int64_t
   for (int p = 0; p < n_shards; ++p)
     for (int64_t i = 0; i < s_n; ++i) pos_out[p * s_n + i] = ra::pos_of(layout, n_shards, s_n, p, i);
   return ok();
+}
+
+ra_status ra_fwd_step(ra_plan_t plan, int32_t step, const void* q, const void* k_blk, const void* v_blk,
+                      float* o_part, float* lse_part, void* stream) {
+  if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
+  const ra_problem& pb = plan->prob;
+  if (step < 0 || step >= pb.n_shards)
+    return fail(RA_ERR_INVALID_ARG, "step %d outside 0..%d", step, pb.n_shards - 1);
+  if (q == nullptr || k_blk == nullptr || v_blk == nullptr || o_part == nullptr || lse_part == nullptr)
+    return fail(RA_ERR_INVALID_ARG, "null pointer");
+  const void* ptrs[] = {q, k_blk, v_blk, o_part, lse_part};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  ra::FwdParams prm = fwd_params(plan);
+  prm.step_lo = (int16_t)step;
+  prm.step_hi = (int16_t)(step + 1);
+  prm.kv_rotated = 1;
+  if (!plan->step_off.empty()) {
+    prm.items = plan->d_step_items + plan->step_off[step];
+    prm.n_items = (int32_t)(plan->step_off[step + 1] - plan->step_off[step]);
+  }
+  prm.o_parts = o_part;
+  prm.lse_parts = lse_part;
+  return launch(plan, prm, q, k_blk, v_blk, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ra_ring_rotate(ra_plan_t plan, const void* k_src, const void* v_src, void* k_dst, void* v_dst,
+                         void* stream) {
+  if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
+  if (k_src == nullptr || v_src == nullptr || k_dst == nullptr || v_dst == nullptr)
+    return fail(RA_ERR_INVALID_ARG, "null pointer");
+  const ra_problem& pb = plan->prob;
+  const size_t bytes = (size_t)pb.batch * pb.heads_kv * pb.seq * pb.head_dim * elem_bytes(pb);
+  if (overlap(k_src, k_dst, bytes) || overlap(v_src, v_dst, bytes) || overlap(k_dst, v_dst, bytes))
+    return fail(RA_ERR_INVALID_ARG, "a destination overlaps its source or the other destination");
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = rotate_one(plan, k_src, k_dst, st);
+  if (e == cudaSuccess) e = rotate_one(plan, v_src, v_dst, st);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "rotation copy failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, void* o, float* lse,
+                      void* k_buf, void* v_buf, float* o_parts, float* lse_parts, void* stream,
+                      void* comm_stream) {
+  if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
+  const ra_problem& pb = plan->prob;
+  const int N = pb.n_shards;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || o_parts == nullptr ||
+      lse_parts == nullptr || (N > 1 && (k_buf == nullptr || v_buf == nullptr)))
+    return fail(RA_ERR_INVALID_ARG, "null pointer");
+  const void* ptrs[] = {q, k, v, o, lse, k_buf, v_buf, o_parts, lse_parts};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+  const size_t kv_bytes = (size_t)pb.batch * pb.heads_kv * pb.seq * pb.head_dim * elem_bytes(pb);
+  if (N > 1 && (overlap(k_buf, v_buf, 2 * kv_bytes) || overlap(k_buf, k, kv_bytes) ||
+                overlap(k_buf, v, kv_bytes) || overlap(v_buf, k, kv_bytes) || overlap(v_buf, v, kv_bytes)))
+    return fail(RA_ERR_INVALID_ARG, "receive buffers overlap each other or K/V");
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(comm_stream);
+  const int64_t rows = pb.batch * (int64_t)pb.heads_q * pb.seq;
+  char* kb = static_cast<char*>(k_buf);
+  char* vb = static_cast<char*>(v_buf);
+  cudaError_t e = cudaSuccess;
+  auto cuda_fail = [&](const char* what) { return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e)); };
+
+  // The communication stream starts after everything already queued on stream
+  // (the caller's writes of K and V, earlier users of the receive buffers).
+  if ((e = cudaEventRecord(plan->ev_entry, st)) != cudaSuccess) return cuda_fail("event record");
+  if ((e = cudaStreamWaitEvent(cs, plan->ev_entry, 0)) != cudaSuccess) return cuda_fail("stream wait");
+  for (int t = 0; t < N; ++t) {
+    // Block held at step t: K/V themselves at step 0, then receive buffer (t - 1) % 2.
+    const void* kt = t == 0 ? k : kb + (size_t)((t - 1) % 2) * kv_bytes;
+    const void* vt = t == 0 ? v : vb + (size_t)((t - 1) % 2) * kv_bytes;
+    if (t >= 1 && (e = cudaStreamWaitEvent(st, plan->ev_rot, 0)) != cudaSuccess) return cuda_fail("stream wait");
+    if (t + 1 < N) {
+      // Pass the block on while step t computes.  Its destination was last read
+      // by step t - 1.
+      if (t >= 2 && (e = cudaStreamWaitEvent(cs, plan->ev_step, 0)) != cudaSuccess) return cuda_fail("stream wait");
+      s = ra_ring_rotate(plan, kt, vt, kb + (size_t)(t % 2) * kv_bytes, vb + (size_t)(t % 2) * kv_bytes, cs);
+      if (s != RA_OK) return s;
+      if ((e = cudaEventRecord(plan->ev_rot, cs)) != cudaSuccess) return cuda_fail("event record");
+    }
+    s = ra_fwd_step(plan, t, q, kt, vt, o_parts + (size_t)t * rows * pb.head_dim, lse_parts + (size_t)t * rows, st);
+    if (s != RA_OK) return s;
+    if ((e = cudaEventRecord(plan->ev_step, st)) != cudaSuccess) return cuda_fail("event record");
+  }
+  return ra_merge_partials(N, rows, pb.head_dim, o_parts, lse_parts, o, pb.dtype, lse, st);
 }
 
 ra_status ra_sync_status(ra_plan_t plan, void* stream) {

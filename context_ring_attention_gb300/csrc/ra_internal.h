@@ -98,20 +98,35 @@ inline bool schedule_before(const ScheduleKey& a, const ScheduleKey& b) {
 }
 inline int64_t schedule_bucket_width(int64_t max_cost) { return max_cost >= 200 ? max_cost / 100 : 1; }
 
+// Kept at 128 bytes: a larger parameter block measurably changes the forward
+// kernel's register allocation (it starts to spill).
 struct FwdParams {
-  int32_t batch, heads_q, heads_kv, group, head_dim, n_shards, layout, causal;
+  int32_t batch, heads_q, heads_kv, group, head_dim, n_shards;
+  int16_t layout, causal;
+  // Ring steps this launch runs, [step_lo, step_hi): 0..N for a whole forward, one
+  // step for a per-step launch.  Partials are indexed t - step_lo.
+  int16_t step_lo, step_hi;
   int64_t seq, s_n;
   int32_t n_items;
   float scale;       // score scale
   float scale_log2;  // scale * log2(e)
+  // 0: the key/value block of step t for query shard p is read in place, at the rows
+  // of shard r = (p - t) mod N.  1: it is read from shard p's own rows of a receive
+  // buffer that holds, in slot p, the block shard p has been passed by step t.
+  int16_t kv_rotated;
+  // 0: CTAs take work items from a counter as they free up.  1: round u gives CTA b
+  // item u*grid + b and starts only when every CTA has issued the previous round's
+  // loads (cooperative launch), so the CTAs of a round stream the same K/V in step.
+  int16_t round_sync;
   const WorkItem* items;
   void* o;           // fused output, plan dtype
   float* lse;        // fused LSE or nullptr
   float* o_parts;    // partials mode outputs or nullptr
   float* lse_parts;
   uint32_t* status;        // device status word (bit set = a wait ran out of budget)
-  uint32_t* item_counter;  // next work item to hand out; zero before each launch
+  uint32_t* item_counter;  // next work item, or rounds issued (round_sync); zero before each launch
 };
+static_assert(sizeof(FwdParams) <= 128, "FwdParams grew past 128 bytes");
 
 // Status bits written by kernels into the plan's status word.
 enum : uint32_t {
@@ -120,6 +135,14 @@ enum : uint32_t {
   kStatusTimeoutSoftmax = 1u << 2,
   kStatusTimeoutTeardown = 1u << 3,
 };
+
+// Whether a bf16 problem runs its forward in synchronised rounds: when one key/value
+// head's K and V (S x d x 2 bytes each) exceed 32 MiB, so that CTAs drifting apart
+// over their items would stream more K/V than L2 holds, and when the longest item
+// (key tiles) stays far below the kernel's wait budget.
+RA_HD bool use_round_sync(int64_t seq, int head_dim, int64_t max_item_tiles) {
+  return seq * head_dim * 4 > (int64_t(32) << 20) && max_item_tiles <= 131072;
+}
 
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, const void* v,

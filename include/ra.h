@@ -35,9 +35,11 @@
  *   - Scores are s = scale * q.k with scale = 1/sqrt(d) unless given.
  *
  * Ownership: the caller owns every device buffer passed in.  A plan owns its
- * host tables, its device work table and its device status word; ra_fwd,
- * ra_merge_partials and ra_layout_perm allocate nothing and are asynchronous on
- * the given stream (a cudaStream_t passed as void*; NULL = legacy default).
+ * host tables, its device work tables (whole forward and one per ring step), its
+ * device status word and three CUDA events; ra_fwd, ra_fwd_step, ra_ring_rotate,
+ * ra_ring_fwd, ra_merge_partials and ra_layout_perm allocate nothing and are
+ * asynchronous on the given stream (a cudaStream_t passed as void*; NULL = legacy
+ * default).
  *
  * Errors: every call returns an ra_status; on failure ra_last_error() returns a
  * thread-local message.  Arguments are checked before anything is launched.
@@ -93,8 +95,9 @@ typedef struct ra_plan_s* ra_plan_t;
  * ra_plan -- validate a problem and build its ring schedule.
  * Builds, on the host, the list of query-tile work items in longest-first order
  * with the per-shard tile classification (FULL / PARTIAL / SKIP, see
- * ra_plan_tile_counts), and, when a CUDA device is current, uploads the work
- * table and allocates the plan's device status word on it.  Without a device
+ * ra_plan_tile_counts) and one list per ring step for ra_fwd_step; when a CUDA
+ * device is current, it uploads the work tables, allocates the plan's device
+ * status word and creates the three events ra_ring_fwd orders its streams with.  Without a device
  * the plan is host-only: tile counts work, ra_fwd returns RA_ERR_NO_DEVICE.
  * *out receives the plan; release it with ra_plan_destroy.
  * Errors: RA_ERR_INVALID_ARG (null pointers, sizes < 1, S % N, zigzag S % 2N,
@@ -138,6 +141,72 @@ ra_status ra_plan_tile_counts(ra_plan_t plan, int64_t* full, int64_t* partial, i
  */
 ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v,
                  void* o, float* lse, float* o_parts, float* lse_parts, void* stream);
+
+/*
+ * ra_fwd_step -- one ring step for every shard, run as the device holding the shard
+ * runs it: each shard attends to the K/V block it holds at that step.
+ * At step t shard p holds the block that started on shard (p - t) mod N, passed
+ * on one device per step (device i -> i+1: "3.6 Distributed Training II",
+ * section "Ring Attention"; the Q&A page, section "The ring").
+ * step: t in [0, N).
+ * q: [B, Hq, S, d] in layout order.
+ * k_blk, v_blk: [B, Hkv, S, d] receive buffers.  The rows of shard p, [p*S/N, (p+1)*S/N),
+ *   hold the block shard p holds at step t: K/V themselves at t = 0, then what t
+ *   calls of ra_ring_rotate have passed along.
+ * o_part [B, Hq, S, d] float32 and lse_part [B, Hq, S] float32 receive the
+ *   attention of every row over that block alone, with the conventions of
+ *   ra_fwd's partials mode: normalised by its own sum; O_t = 0 and LSE_t = -inf
+ *   where the block has no causal key.  The result equals entry t of ra_fwd's
+ *   partials.
+ * Device pointers in the plan's dtype (o_part/lse_part float32), 16-byte aligned.
+ * Asynchronous on stream; allocates nothing; the plan holds one work list per step.
+ * Calls that share a plan must not overlap on the GPU.
+ * Errors: RA_ERR_INVALID_ARG (step out of range, null/misaligned pointers),
+ * RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ */
+ra_status ra_fwd_step(ra_plan_t plan, int32_t step, const void* q, const void* k_blk,
+                      const void* v_blk, float* o_part, float* lse_part, void* stream);
+
+/*
+ * ra_ring_rotate -- the ring's exchange, in which every shard passes its K/V block on
+ * to the next: for each [S, d] matrix of K and V ([B, Hkv, S, d], plan dtype), the
+ * rows of shard (p + 1) mod N in the destination receive the rows of shard p in the
+ * source (device i -> i+1; "3.6 Distributed Training II", "Ring Attention").
+ * The copies are copy-engine transfers, two per tensor (strided over B*Hkv), so
+ * they can run on a second stream while a forward kernel occupies every SM.  That
+ * is one GPU's stand-in for the send/receive that overlaps compute between devices.
+ * k_src, v_src, k_dst, v_dst: device pointers.  A destination must not overlap its
+ * source or the other destination.  Asynchronous on stream; allocates nothing.
+ * Errors: RA_ERR_INVALID_ARG (null pointers, overlap), RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ */
+ra_status ra_ring_rotate(ra_plan_t plan, const void* k_src, const void* v_src, void* k_dst,
+                         void* v_dst, void* stream);
+
+/*
+ * ra_ring_fwd -- the explicit ring driver.  It runs N calls of ra_fwd_step on
+ * `stream`.  While step t computes, ra_ring_rotate passes the block of step t on
+ * to the receive buffer of step t+1, on `comm_stream`: the overlap of
+ * communication with compute that "3.6 Distributed Training II", "Ring
+ * Attention", describes.  Then it merges the N partials with ra_merge_partials
+ * (Module 23, "The Math: One Block at a Time": the fold is order independent).
+ * q, k, v: as for ra_fwd.
+ * o [B, Hq, S, d] (plan dtype) and lse [B, Hq, S] float32 (may be NULL) receive
+ *   the fused result.
+ * k_buf, v_buf: caller-owned scratch, two receive buffers each: [2, B, Hkv, S, d]
+ *   in the plan's dtype.  They must not overlap each other or K/V.  May be NULL
+ *   when N == 1.
+ * o_parts [N, B, Hq, S, d] and lse_parts [N, B, Hq, S]: caller-owned float32
+ *   scratch for the per-step partials; they hold them after the call.
+ * stream: the compute stream.  comm_stream: the rotation stream; it may equal
+ *   stream, and then nothing overlaps.  The driver orders both streams with three
+ *   events that the plan owns.  Work already queued on stream comes before the
+ *   rotations; later work on stream comes after the driver's work on both streams.
+ * Asynchronous; allocates nothing.  Calls that share a plan must not overlap.
+ * Errors: as ra_fwd_step, ra_ring_rotate and ra_merge_partials.
+ */
+ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, void* o,
+                      float* lse, void* k_buf, void* v_buf, float* o_parts, float* lse_parts,
+                      void* stream, void* comm_stream);
 
 /*
  * ra_merge_partials -- exact combination of partial attention results.

@@ -122,3 +122,39 @@ def test_tile_counts_seq32k_report():
             assert len(set((full + part).tolist())) == 1          # exactly balanced
         else:
             assert (full + part).tolist() == sorted((full + part).tolist())
+
+
+def test_ring_entry_points_check_arguments(lib):
+    """Argument checks of ra_fwd_step / ra_ring_rotate / ra_ring_fwd (no launch)."""
+    plan = ra.ra_plan(1, 1024, 4, 2, 128, 4, "zigzag", True, "bf16")
+    a = 1 << 20                      # aligned fake device addresses: nothing is dereferenced
+    kv = 1 * 2 * 1024 * 128 * 2      # bytes of one K or V
+    h = plan.handle
+    assert lib.ra_fwd_step(h, 4, a, a, a, a, a, None) == 1          # step out of range
+    assert lib.ra_fwd_step(h, -1, a, a, a, a, a, None) == 1
+    assert lib.ra_fwd_step(h, 0, None, a, a, a, a, None) == 1       # null q
+    assert lib.ra_fwd_step(h, 0, a + 8, a, a, a, a, None) == 1      # misaligned
+    assert lib.ra_fwd_step(None, 0, a, a, a, a, a, None) == 1
+    assert lib.ra_ring_rotate(h, a, a + 4 * kv, None, a + 6 * kv, None) == 1       # null destination
+    assert lib.ra_ring_rotate(h, a, a + 4 * kv, a + 16, a + 6 * kv, None) == 1     # dst overlaps src
+    assert lib.ra_ring_rotate(h, a, a + 4 * kv, a + 2 * kv, a + 2 * kv + 16, None) == 1  # dsts overlap
+    assert "overlaps" in ra.ra_last_error()
+    k, v, kb, vb = a, a + kv, a + 2 * kv, a + 4 * kv
+    assert lib.ra_ring_fwd(h, a, k, v, a, None, None, vb, a, a, None, None) == 1   # N > 1 needs k_buf
+    assert lib.ra_ring_fwd(h, a, k, v, a, None, kb, kb + kv, a, a, None, None) == 1  # k_buf/v_buf overlap
+    assert lib.ra_ring_fwd(h, a, k, v, a, None, k, vb, a, a, None, None) == 1      # k_buf overlaps K
+    assert lib.ra_ring_fwd(h, a, k, v, None, None, kb, vb, a, a, None, None) == 1  # null o
+    pytest.importorskip("torch")
+    import torch
+    if torch.cuda.is_available():
+        return
+    # well-formed calls on a plan without a device
+    assert lib.ra_fwd_step(h, 3, a, a, a, a, a, None) == 5
+    assert lib.ra_ring_rotate(h, a, a + 2 * kv, a + 4 * kv, a + 6 * kv, None) == 5
+    assert lib.ra_ring_fwd(h, a, k, v, a, None, kb, vb, a, a, None, None) == 5
+
+
+def test_plan_rejects_too_many_shards(lib):
+    with pytest.raises(ra.RaError) as ei:
+        ra.ra_plan(1, 65536, 1, 1, 128, 32768, "contiguous", False, "bf16")
+    assert ei.value.status == 2
