@@ -37,6 +37,10 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
 ``pass_blocks``,            after t exchanges slot p holds the block that started in slot
 ``held_blocks``             (p - t) mod N (labelled rows); N exchanges are the identity;
                             attention over the held block equals ``ring_partials`` entry t.
+``attention_backward``      central finite differences of ``full_attention`` (float64) on tiny
+                            cases, causal and not, with grouped heads; a single key gives
+                            dV = dO and dQ = dK = 0; the rows of dK sum to zero.
+``ring_backward``           equals ``attention_backward`` for every layout, causal and not.
 ``merge_partials``          splitting the keys into halves and merging reproduces
                             ``full_attention``; -inf parts are ignored.
 ``tile_counts``             brute force over every (q, k) pair of every tile on small
@@ -50,6 +54,7 @@ from .layouts import CONTIGUOUS, STRIPED, ZIGZAG, LAYOUTS, layout_positions, cau
 from .attention import attention_rows, full_attention, full_attention_rows
 from .ring import ring_sim, ring_partials, pass_blocks, held_blocks
 from .merge import merge_partials
+from .backward import attention_backward, ring_backward
 from .tiles import tile_counts, tile_classes_bruteforce
 
 __all__ = [
@@ -57,5 +62,6 @@ __all__ = [
     "layout_positions", "causal_pair_counts",
     "full_attention", "full_attention_rows", "attention_rows",
     "ring_sim", "ring_partials", "pass_blocks", "held_blocks", "merge_partials",
+    "attention_backward", "ring_backward",
     "tile_counts", "tile_classes_bruteforce",
 ]

@@ -375,3 +375,60 @@ def test_held_blocks_give_ring_partials(layout):
                 ok = np.isfinite(l)
                 np.testing.assert_allclose(o[ok], op[t, 0, h, rows][ok], atol=1e-13)
                 np.testing.assert_allclose(l, lp[t, 0, h, rows], atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# Backward pass
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_finite_differences(causal):
+    # L = sum(O * dO); its gradient by central differences of full_attention
+    B, Hq, Hkv, S, d = 1, 2, 1, 6, 3
+    q, k, v, do = _rand((B, Hq, S, d), 70), _rand((B, Hkv, S, d), 71), _rand((B, Hkv, S, d), 72), _rand((B, Hq, S, d), 73)
+    pos = layout_positions(ZIGZAG, S, 3)            # rows in a layout order, masked by position
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=causal, positions=pos)
+
+    def loss(q_, k_, v_):
+        o, _ = full_attention(q_, k_, v_, causal=causal, positions=pos)
+        return float((o * do).sum())
+
+    eps = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(**{a + "_": t for a, t in args_p.items()}) -
+                        loss(**{a + "_": t for a, t in args_m.items()})) / (2 * eps)
+        np.testing.assert_allclose(g, num, atol=1e-7, rtol=1e-6, err_msg=name)
+
+
+def test_backward_special_cases():
+    # one key: O = v, so dV = dO and nothing flows to q or k
+    q, k, v, do = _rand((1, 1, 1, 4), 80), _rand((1, 1, 1, 4), 81), _rand((1, 1, 1, 4), 82), _rand((1, 1, 1, 4), 83)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do)
+    np.testing.assert_allclose(dv, do, atol=1e-15)
+    assert np.all(dq == 0) and np.all(dk == 0)
+    # softmax rows sum to one, so each row of dS sums to zero and the rows of dK sum to zero
+    q, k, v, do = _rand((1, 2, 16, 4), 84), _rand((1, 1, 16, 4), 85), _rand((1, 1, 16, 4), 86), _rand((1, 2, 16, 4), 87)
+    for causal in (False, True):
+        _, dk, _ = oracle.attention_backward(q, k, v, do, causal=causal)
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ring_backward_equals_attention_backward(layout, causal):
+    B, Hq, Hkv, S, d, n = 1, 4, 2, 24, 4, 3
+    q, k, v, do = _rand((B, Hq, S, d), 90), _rand((B, Hkv, S, d), 91), _rand((B, Hkv, S, d), 92), _rand((B, Hq, S, d), 93)
+    pos = layout_positions(layout, S, n)
+    o, lse = full_attention(q, k, v, causal=causal, positions=pos)
+    want = oracle.attention_backward(q, k, v, do, causal=causal, positions=pos)
+    got = oracle.ring_backward(q, k, v, do, o, lse, n, positions=pos, causal=causal)
+    for g, w in zip(got, want):
+        np.testing.assert_allclose(g, w, atol=1e-12)
