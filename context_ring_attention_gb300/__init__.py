@@ -1,7 +1,7 @@
 """GB300 ring-attention forward: Python binding of libra.so (include/ra.h).
 
 The functions keep the C names (``ra_plan``, ``ra_fwd``, ``ra_fwd_step``,
-``ra_ring_rotate``, ``ra_ring_fwd``, ``ra_merge_partials``, ``ra_layout_perm``,
+``ra_ring_rotate``, ``ra_ring_fwd``, ``ra_bwd``, ``ra_merge_partials``, ``ra_layout_perm``,
 ``ra_layout_index``, ``ra_plan_tile_counts``, ``ra_sync_status``,
 ``ra_last_error``, ``ra_fwd_static``).  This module only marshals arguments:
 PyTorch supplies device memory and the current stream, every step of the
@@ -21,7 +21,7 @@ __all__ = [
     "RaError", "Plan", "LAYOUTS",
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-    "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd",
+    "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -31,7 +31,7 @@ _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_
            4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd")
+            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -79,6 +79,7 @@ def load_library():
         "ra_fwd_step": ([P, I32, VP, VP, VP, VP, VP, VP], I32),
         "ra_ring_rotate": ([P, VP, VP, VP, VP, VP], I32),
         "ra_ring_fwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
+        "ra_bwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -338,3 +339,30 @@ def ra_ring_fwd(plan, q, k, v, o=None, lse=None, k_buf=None, v_buf=None, o_parts
                                       _ptr(v_buf), _ptr(o_parts), _ptr(lse_parts), _stream(stream),
                                       _stream(comm_stream)))
     return o, lse
+
+
+def ra_bwd(plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scratch=None, stream=None):
+    """Gradients (dQ, dK, dV) of the forward for the upstream gradient ``dout``.
+
+    ``o`` and ``lse`` are the forward's outputs for the same q, k, v; ``scratch``
+    (4 * B * Hq * S float32) is allocated here unless passed in.
+    """
+    import torch
+    pb = plan.problem
+    B, Hq, S = pb["batch"], pb["heads_q"], pb["seq"]
+    _check_qkv(plan, q=q, k=k, v=v)
+    _check_qkv(plan, q=o)
+    _check_qkv(plan, q=dout)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    if scratch is None:
+        scratch = torch.empty((B, Hq, S, 4), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, S):
+        raise ValueError("lse must be a contiguous float32 tensor of shape (B, Hq, S)")
+    _check(load_library().ra_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(scratch), _stream(stream)))
+    return dq, dk, dv

@@ -1,0 +1,697 @@
+// Ring-attention backward, bf16, d = 128, on the sm_100-family tensor cores.
+//
+// What it computes.  The pages print no backward pass; this kernel differentiates
+// the forward's definition (Module 23, "The Math: One Block at a Time";
+// "3.6 Distributed Training II", section "Ring Attention").  With the forward's
+// LSE the probabilities are recomputed tile by tile,
+//   P = 2^(scale*log2(e) * q.k - LSE*log2(e)),   dP = dO V^T,
+//   dS = P * (dP - D)   with D = rowsum(dO * O),
+//   dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K,
+// and a key/value head's dK, dV gather the contributions of every query head of
+// its group.  Two passes of one kernel template:
+//   pass 0 (dK, dV): a work item is one 128-row key tile of shard r.  Its block
+//     travels the ring: at step t it sits on the device of shard (r + t) mod N and
+//     meets that shard's query tiles (every query head of the group in turn), so
+//     the block's gradients gather where the block goes.
+//   pass 1 (dQ): a work item is one 128-row query tile of shard p; it meets the
+//     key blocks of shards (p - t) mod N in the forward's ring order.
+// Causal: only the query tiles that see some key of the tile (pass 0), or the key
+// tiles some query of the tile sees (pass 1), are visited; the rest of the mask
+// is applied per element by global position (Module 23, "Exact by Construction").
+//
+// How (one persistent CTA per SM, 12 warps):
+//   warp 0     TMA producer: the item's two 128-row tiles (K, V in pass 0; Q, dO
+//              in pass 1) once, then 64-row tiles of the other two tensors (Q, dO
+//              and 64 {LSE*log2(e), D} rows in pass 0; K, V in pass 1) into a ring
+//              of stages.
+//   warp 1     tcgen05 issuer (converged warp, one elected lane):
+//              per streamed tile two SS MMAs (M = 128, N = 64) give the scores and
+//              dP (pass 0 transposed: keys are the TMEM lanes), then TS MMAs
+//              (M = 128, N = 128, K = 64) add P^T dO and dS^T Q (pass 0) or dS K
+//              (pass 1) into accumulators, reading P and dS from tensor memory and
+//              the streamed tile, still in shared memory, as an MN-major operand.
+//   warps 4-7 / 8-11  elementwise: one thread per TMEM lane turns scores and dP
+//              into P and dS (bf16, written back into tensor memory), for the
+//              even / odd tiles of an item; at the end of an item they write the
+//              accumulators (pass 0: warps 4-7 dV, 8-11 dK; pass 1: half of dQ each).
+// TMEM: two tile buffers of 128 columns (scores 0-63, dP 64-127; P over 0-31 and
+// dS over 64-95 once computed), accumulators at 256-383 and 384-511.
+// Every wait is bounded (~1 s); on expiry the CTA records it in the status word,
+// drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ra_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kRegsLaunch = 168;
+constexpr uint32_t kRegsOther = 120;
+constexpr uint32_t kRegsCompute = 192;
+static_assert(128 * kRegsOther + 256 * kRegsCompute <= kThreads * kRegsLaunch, "register split");
+
+constexpr int kFixRows = 128;                     // rows of the item's own tiles
+constexpr int kStreamRows = 64;                   // rows of a streamed tile
+constexpr uint32_t kFixBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
+constexpr uint32_t kFixHalf = 128 * 64 * 2;       // its 128-byte swizzle column
+constexpr uint32_t kStrBytes = 64 * 128 * 2;      // one 64 x 128 bf16 tile
+constexpr uint32_t kStrHalf = 64 * 64 * 2;
+constexpr uint32_t kLseBytes = 64 * 16;           // 64 rows of float4 {lse2, D, 0, 0}
+
+template <int kPass>
+struct Cfg {
+  static constexpr int kStages = kPass == 0 ? 4 : 5;
+  static constexpr uint32_t kStageBytes = kPass == 0 ? 2 * kStrBytes + 1024 : 2 * kStrBytes;
+  static constexpr uint32_t kOffFix = 0;
+  static constexpr uint32_t kOffStage = 2 * kFixBytes;
+  static constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
+  static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+};
+
+enum : int {
+  kFixFull = 0,
+  kFixEmpty = 1,
+  kAccFull = 2,
+  kAccEmpty = 3,
+  kDone = 4,
+  kSFull = 5,       // 2
+  kPFull = 7,       // 2
+  kItemFull = 9,    // 4
+  kItemEmpty = 13,  // 4
+  kStFull = 17,     // kStages
+};
+template <int kPass>
+struct Bars {
+  static constexpr int kStEmpty = kStFull + Cfg<kPass>::kStages;
+  static constexpr int kNum = kStEmpty + Cfg<kPass>::kStages;
+};
+constexpr int kItemSlots = 4;
+constexpr uint32_t kItemConsumers = 9;  // MMA warp + 8 elementwise warps
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColAcc0 = 256, kColAcc1 = 384;
+__device__ __forceinline__ uint32_t col_buf(int b) { return b ? 128u : 0u; }
+constexpr uint32_t kColDP = 64;   // dP within a buffer; dS is written over its first 32 columns
+constexpr uint32_t kIdescSS = ptx::idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t kIdescTS = ptx::idesc_bf16_f32(128, 128, false, true);
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;
+constexpr uint32_t kSuspendHintNs = 2000u;
+
+struct Ctl {
+  uint32_t bars;
+  volatile uint32_t* abort;
+  uint32_t* status;
+  __device__ __forceinline__ uint32_t bar(int i) const { return bars + 8u * (uint32_t)i; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Ctl& c, uint32_t bar, uint32_t parity, uint32_t who) {
+  if (ptx::mbar_test(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_wait_hint(bar, parity, kSuspendHintNs)) return true;
+    if ((it & 15u) == 0) {
+      if (*c.abort) return false;
+      if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
+        *c.abort = 1u;
+        atomicOr(c.status, who);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void drain_bar(const Ctl& c, uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (!ptx::mbar_test(bar, parity)) {
+    if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
+      atomicOr(c.status, kStatusTimeoutTeardown);
+      return;
+    }
+  }
+}
+
+// ------------------------------------------------------------------- walks --
+// The streamed tiles of an item, in order.  Pass 0 (item = key tile of shard r
+// whose first key sits at position kmin): ring step t puts the block on shard
+// p = (r + t) mod N; every query head g of the group; query tiles it of shard p
+// from the first that sees key position kmin.  Pass 1 (item = query tile of shard
+// p whose last query sits at position maxq): step t meets shard r = (p - t) mod N,
+// key tiles 0..last_le(r, maxq)/64.
+struct Walk {
+  int t, g, it, lo, hi, shard;
+};
+
+__device__ __forceinline__ int n_stream_tiles(const BwdParams& P) {
+  return (int)((P.s_n + kStreamRows - 1) / kStreamRows);
+}
+
+template <int kPass>
+__device__ __forceinline__ void walk_step_bounds(Walk& w, const BwdParams& P, const WorkItem& it) {
+  const int N = P.n_shards;
+  if (kPass == 0) {
+    w.shard = (it.shard + w.t) % N;
+    w.hi = n_stream_tiles(P);
+    w.lo = 0;
+    if (P.causal) {  // first query of the shard that sees the tile's first key, if any
+      const int64_t f = first_ge(P.layout, N, P.s_n, w.shard, it.maxq);
+      w.lo = f >= P.s_n ? w.hi : (int)(f / kStreamRows);
+    }
+  } else {
+    w.shard = (it.shard - w.t + N) % N;
+    w.lo = 0;
+    if (P.causal) {
+      const int64_t j = last_le(P.layout, N, P.s_n, w.shard, it.maxq);
+      w.hi = j < 0 ? 0 : (int)(j / kStreamRows) + 1;
+    } else {
+      w.hi = n_stream_tiles(P);
+    }
+  }
+}
+
+// Advance to the next non-empty (t, g) range starting at the current one.
+template <int kPass>
+__device__ __forceinline__ void walk_settle(Walk& w, const BwdParams& P, const WorkItem& it) {
+  const int groups = kPass == 0 ? P.group : 1;
+  while (w.t < P.n_shards) {
+    if (w.it < w.hi) return;
+    if (++w.g < groups) {
+      w.it = w.lo;
+      continue;
+    }
+    w.g = 0;
+    if (++w.t >= P.n_shards) return;
+    walk_step_bounds<kPass>(w, P, it);
+    w.it = w.lo;
+  }
+}
+
+template <int kPass>
+__device__ __forceinline__ void walk_begin(Walk& w, const BwdParams& P, const WorkItem& it) {
+  w.t = 0;
+  w.g = 0;
+  walk_step_bounds<kPass>(w, P, it);
+  w.it = w.lo;
+  walk_settle<kPass>(w, P, it);
+}
+
+template <int kPass>
+__device__ __forceinline__ void walk_next(Walk& w, const BwdParams& P, const WorkItem& it) {
+  ++w.it;
+  walk_settle<kPass>(w, P, it);
+}
+
+// Number of streamed tiles of an item (the walk's length).
+template <int kPass>
+__device__ __forceinline__ int item_tiles(const BwdParams& P, const WorkItem& it) {
+  int n = 0;
+  Walk w;
+  for (w.t = 0; w.t < P.n_shards; ++w.t) {
+    walk_step_bounds<kPass>(w, P, it);
+    if (w.hi > w.lo) n += (w.hi - w.lo) * (kPass == 0 ? P.group : 1);
+  }
+  return n;
+}
+
+__device__ __forceinline__ int next_item(const Ctl& c, volatile int32_t* slots, uint32_t u, int lane) {
+  const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
+  if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kItemFull + (int)slot), use & 1u, kStatusTimeoutSoftmax)))
+    return -1;
+  const int idx = slots[slot];
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(c.bar(kItemEmpty + (int)slot));
+  return idx;
+}
+
+// ---------------------------------------------------------------- producer --
+struct ProducerState {
+  uint32_t str_issued;  // streamed tiles issued
+  uint32_t fix_issued;  // items whose own tiles were issued
+};
+
+template <int kPass>
+__device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
+                             const CUtensorMap* tx0, const CUtensorMap* tx1, const CUtensorMap* ty0,
+                             const CUtensorMap* ty1, const CUtensorMap* tl, ProducerState& st) {
+  using C = Cfg<kPass>;
+  const int lane = threadIdx.x & 31;
+  const uint64_t keep = ptx::l2_policy_evict_last();
+  uint32_t s_it = 0;
+  for (uint32_t u = 0;; ++u) {
+    const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kItemEmpty + (int)slot), (use & 1u) ^ 1u, kStatusTimeoutProducer)))
+      break;
+    int idx = 0;
+    if (lane == 0) idx = (int)atomicAdd(P.item_counter, 1u);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    if (idx >= P.n_items) idx = -1;
+    if (lane == 0) slots[slot] = idx;
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
+    if (idx < 0) break;
+    const WorkItem it = P.items[idx];
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
+    // The item's own tiles: rows bh0*S + shard*s_n + row0 of K and V (pass 0) or Q and dO (pass 1).
+    const int32_t yf = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
+    ptx::mbar_arrive_expect_tx_warp(c.bar(kFixFull), 2 * kFixBytes);
+    ptx::tma_load_2d_warp(sbase + C::kOffFix, tx0, c.bar(kFixFull), 0, yf);
+    ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixHalf, tx0, c.bar(kFixFull), 64, yf);
+    ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixBytes, tx1, c.bar(kFixFull), 0, yf);
+    ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixBytes + kFixHalf, tx1, c.bar(kFixFull), 64, yf);
+    st.fix_issued = u + 1;
+    // Streamed tiles.
+    int b, h_base;
+    if (kPass == 0) {  // bh0 = b * Hkv + kv head; queries of heads kv*G .. kv*G + G-1
+      b = it.bh0 / P.heads_kv;
+      h_base = (it.bh0 % P.heads_kv) * P.group;
+    } else {           // bh0 = b * Hq + h; its key/value head
+      b = it.bh0 / P.heads_q;
+      h_base = (it.bh0 % P.heads_q) / P.group;
+    }
+    Walk w;
+    walk_begin<kPass>(w, P, it);
+    bool ok = true;
+    while (w.t < P.n_shards) {
+      const int64_t head_row = kPass == 0 ? ((int64_t)b * P.heads_q + h_base + w.g) * P.seq
+                                          : ((int64_t)b * P.heads_kv + h_base) * P.seq;
+      const int32_t y = (int32_t)(head_row + (int64_t)w.shard * P.s_n + (int64_t)w.it * kStreamRows);
+      const uint32_t s = s_it % C::kStages, phase = (s_it / C::kStages) & 1u;
+      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kStFull + C::kStages + (int)s), phase ^ 1u, kStatusTimeoutProducer))) {
+        ok = false;
+        break;
+      }
+      const uint32_t dst = sbase + C::kOffStage + s * C::kStageBytes;
+      ptx::mbar_arrive_expect_tx_warp(c.bar(kStFull + (int)s), kPass == 0 ? 2 * kStrBytes + kLseBytes : 2 * kStrBytes);
+      ptx::tma_load_2d_warp_hint(dst, ty0, c.bar(kStFull + (int)s), 0, y, keep);
+      ptx::tma_load_2d_warp_hint(dst + kStrHalf, ty0, c.bar(kStFull + (int)s), 64, y, keep);
+      ptx::tma_load_2d_warp_hint(dst + kStrBytes, ty1, c.bar(kStFull + (int)s), 0, y, keep);
+      ptx::tma_load_2d_warp_hint(dst + kStrBytes + kStrHalf, ty1, c.bar(kStFull + (int)s), 64, y, keep);
+      if (kPass == 0) ptx::tma_load_2d_warp(dst + 2 * kStrBytes, tl, c.bar(kStFull + (int)s), 0, y);
+      st.str_issued = ++s_it;
+      walk_next<kPass>(w, P, it);
+    }
+    if (!ok) break;
+  }
+}
+
+// --------------------------------------------------------------------- MMA --
+template <int kPass>
+__device__ __forceinline__ void issue_ss(uint32_t tmem, int buf, uint32_t fix_lo, uint32_t str_lo) {
+  // Scores: fixed tile 0 x streamed tile 0; dP: fixed tile 1 x streamed tile 1.
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const uint32_t a0 = fix_lo + (which ? (kFixBytes >> 4) : 0u);
+    const uint32_t b0 = str_lo + (which ? (kStrBytes >> 4) : 0u);
+    const uint32_t d = tmem + col_buf(buf) + (which ? kColDP : 0u);
+#pragma unroll
+    for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of K = 16 over d = 128
+      const uint32_t oa = ((kk >> 2) * kFixHalf + (kk & 3u) * 32u) >> 4;
+      const uint32_t ob = ((kk >> 2) * kStrHalf + (kk & 3u) * 32u) >> 4;
+      ptx::mma_bf16_ss_lo_warp(d, a0 + oa, b0 + ob, kIdescSS, kk > 0 ? 1u : 0u);
+    }
+  }
+}
+
+// acc += A[tmem, 64 K-columns as 32 words] * B[streamed 64-row tile, MN-major].
+__device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t b_lo, bool accumulate) {
+#pragma unroll
+  for (uint32_t kk = 0; kk < 4; ++kk)  // 4 steps of 16 rows = 8 TMEM columns of A
+    ptx::mma_bf16_ts_lo_warp(d, a_tmem + kk * 8u, b_lo + ((kk * 2048u) >> 4), kIdescTS,
+                             (accumulate || kk > 0) ? 1u : 0u);
+}
+
+template <int kPass>
+__device__ void run_mma(const BwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots, uint32_t tmem) {
+  using C = Cfg<kPass>;
+  const int lane = threadIdx.x & 31;
+  const uint32_t fix_lo = ptx::desc_lo(sbase + C::kOffFix, 16);
+  uint32_t s_it = 0, pj[2] = {0, 0};
+  for (uint32_t u = 0;; ++u) {
+    const int idx = next_item(c, slots, u, lane);
+    if (idx < 0) break;
+    const WorkItem it = P.items[idx];
+    const int n = item_tiles<kPass>(P, it);
+    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixFull), u & 1u, kStatusTimeoutMma))) return;
+    auto str_lo = [&](uint32_t i, uint32_t lbo) {
+      return ptx::desc_lo(sbase + C::kOffStage + ((s_it + i) % C::kStages) * C::kStageBytes, lbo);
+    };
+    auto wait_stage = [&](uint32_t i) {
+      return __all_sync(0xffffffffu, wait_bar(c, c.bar(kStFull + (int)((s_it + i) % C::kStages)),
+                                              ((s_it + i) / C::kStages) & 1u, kStatusTimeoutMma));
+    };
+    if (n > 0) {
+      if (!wait_stage(0)) return;
+      issue_ss<kPass>(tmem, 0, fix_lo, str_lo(0, 16));
+      ptx::mma_commit_warp(c.bar(kSFull + 0));
+    }
+    for (int i = 0; i < n; ++i) {
+      const int b = i & 1;
+      if (i + 1 < n) {  // next tile's scores and dP into the other buffer
+        if (!wait_stage((uint32_t)i + 1)) return;
+        issue_ss<kPass>(tmem, b ^ 1, fix_lo, str_lo((uint32_t)i + 1, 16));
+        ptx::mma_commit_warp(c.bar(kSFull + (b ^ 1)));
+      }
+      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kPFull + b), pj[b] & 1u, kStatusTimeoutMma))) return;
+      ++pj[b];
+      if (i == 0 && u > 0 &&
+          !__all_sync(0xffffffffu, wait_bar(c, c.bar(kAccEmpty), (u - 1) & 1u, kStatusTimeoutMma)))
+        return;
+      ptx::tc_fence_after();
+      // Streamed tile 0 (Q in pass 0, K in pass 1) and tile 1 (dO) as MN-major B.
+      const uint32_t y0 = str_lo((uint32_t)i, kStrHalf), y1 = y0 + (kStrBytes >> 4);
+      const uint32_t buf = tmem + col_buf(b);
+      if (kPass == 0) {
+        issue_ts(tmem + kColAcc0, buf, y1, i > 0);           // dV += P^T dO
+        issue_ts(tmem + kColAcc1, buf + kColDP, y0, i > 0);  // dK += dS^T Q
+      } else {
+        issue_ts(tmem + kColAcc0, buf + kColDP, y0, i > 0);  // dQ += dS K
+      }
+      ptx::mma_commit_warp(c.bar(kStFull + C::kStages + (int)((s_it + (uint32_t)i) % C::kStages)));
+    }
+    if (n == 0 && u > 0 &&
+        !__all_sync(0xffffffffu, wait_bar(c, c.bar(kAccEmpty), (u - 1) & 1u, kStatusTimeoutMma)))
+      return;
+    ptx::mma_commit_warp(c.bar(kAccFull));
+    ptx::mma_commit_warp(c.bar(kFixEmpty));
+    s_it += (uint32_t)n;
+  }
+}
+
+// -------------------------------------------------------------- elementwise --
+// Write 64 accumulator columns [col0, col0 + 64) of this thread's row, times mul,
+// as bf16 (zeros when the item met no tile).
+__device__ __forceinline__ void store_row(uint32_t t_acc, uint16_t* dst_row, int col0, float mul, bool valid,
+                                          bool zero) {
+#pragma unroll 1
+  for (int cc = 0; cc < 2; ++cc) {
+    uint32_t v[32];
+    __syncwarp();
+    ptx::tmem_ld32(t_acc + (uint32_t)(col0 + cc * 32), v);
+    if (valid) {
+      uint4* d = reinterpret_cast<uint4*>(dst_row + col0 + cc * 32);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = zero ? 0u
+                      : ptx::pack_bf16x2(__uint_as_float(v[8 * q + 2 * e]) * mul,
+                                         __uint_as_float(v[8 * q + 2 * e + 1]) * mul);
+        d[q] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
+template <int kPass>
+__device__ void run_elementwise(const BwdParams& P, const Ctl& c, const uint8_t* sgen, volatile int32_t* slots,
+                                uint32_t tmem, int g, int wq, int lane) {
+  using C = Cfg<kPass>;
+  const int row = wq * 32 + lane;  // TMEM lane: key row (pass 0) or query row (pass 1)
+  const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+  const int N = P.n_shards;
+  const float sl2 = P.scale_log2;
+  uint32_t s_it = 0, sj = 0;
+  for (uint32_t u = 0;; ++u) {
+    const int idx = next_item(c, slots, u, lane);
+    if (idx < 0) break;
+    const WorkItem it = P.items[idx];
+    const int n = item_tiles<kPass>(P, it);
+    const int64_t i_own = (int64_t)it.row0 + row;  // local row of the item's own tile
+    const bool valid = i_own < P.s_n;
+    const int64_t my_pos = pos_of(P.layout, N, P.s_n, it.shard, valid ? i_own : P.s_n - 1);
+    const int64_t out_row = (int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + i_own;
+    float2 own = make_float2(0.f, 0.f);  // pass 1: this query row's {lse2, D}
+    if (kPass == 1 && valid) {
+      const float4 t4 = P.lse2d[out_row];
+      own = make_float2(t4.x, t4.y);
+    }
+
+    Walk w;
+    walk_begin<kPass>(w, P, it);
+    for (int i = 0; i < n; ++i) {
+      const int64_t tile_lo = (int64_t)w.it * kStreamRows;  // first local row of the streamed tile
+      const int shard = w.shard;
+      const uint32_t stage = (s_it + (uint32_t)i) % C::kStages;
+      walk_next<kPass>(w, P, it);
+      if ((i & 1) != g) continue;
+      // Columns [c_lo, c_hi) of this tile are live for this row.
+      int c_lo = 0;
+      const int64_t left = P.s_n - tile_lo;
+      int c_hi = left < kStreamRows ? (int)left : kStreamRows;
+      if (P.causal) {
+        if (kPass == 0) {  // queries of `shard` at or after this key's position
+          const int64_t f = first_ge(P.layout, N, P.s_n, shard, my_pos) - tile_lo;
+          c_lo = f < 0 ? 0 : (f > kStreamRows ? kStreamRows : (int)f);
+        } else {           // keys of `shard` at or before this query's position
+          const int64_t l = last_le(P.layout, N, P.s_n, shard, my_pos) - tile_lo + 1;
+          const int lim = l < 0 ? 0 : (l > kStreamRows ? kStreamRows : (int)l);
+          c_hi = lim < c_hi ? lim : c_hi;
+        }
+      }
+      const bool ok = wait_bar(c, c.bar(kSFull + g), sj & 1u, kStatusTimeoutSoftmax);
+      ++sj;
+      if (!__all_sync(0xffffffffu, ok)) return;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem + lane_off + col_buf(g);
+      uint32_t raw[128];  // scores in 0-63, dP in 64-127
+      ptx::tmem_ld128(tb, raw);
+      // pass 0: the tile's queries' {lse2, D}, streamed with it (float4 rows)
+      const float4* lse_tile =
+          reinterpret_cast<const float4*>(sgen + C::kOffStage + stage * C::kStageBytes + 2 * kStrBytes);
+      uint32_t pw[32], dw[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float pv[2], dsv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cc = 2 * e + h;
+          const float2 ld = kPass == 0 ? *reinterpret_cast<const float2*>(lse_tile + cc) : own;
+          const float sc = __uint_as_float(raw[cc]);
+          const float dp = __uint_as_float(raw[64 + cc]);
+          const bool live = cc >= c_lo && cc < c_hi;
+          const float pr = live ? ptx::ex2_approx(fmaf(sc, sl2, -ld.x)) : 0.f;
+          pv[h] = pr;
+          dsv[h] = pr * (dp - ld.y);
+        }
+        pw[e] = ptx::pack_bf16x2(pv[0], pv[1]);
+        dw[e] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+      }
+      if (kPass == 0) ptx::tmem_st32(tb, pw);  // P^T for dV (pass 1 needs only dS)
+      ptx::tmem_st32(tb + kColDP, dw);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(kPFull + g));
+    }
+    s_it += (uint32_t)n;
+
+    // Item done: write the accumulators (pass 0: dV by warps 4-7, dK by 8-11;
+    // pass 1: dQ columns 0-63 by warps 4-7, 64-127 by 8-11).
+    const bool ok = wait_bar(c, c.bar(kAccFull), u & 1u, kStatusTimeoutSoftmax);
+    if (!__all_sync(0xffffffffu, ok)) return;
+    ptx::tc_fence_after();
+    if (kPass == 0) {
+      uint16_t* dst = static_cast<uint16_t*>(g ? P.dk : P.dv) + out_row * 128;
+      const uint32_t t_acc = tmem + lane_off + (g ? kColAcc1 : kColAcc0);
+      store_row(t_acc, dst, 0, g ? P.scale : 1.0f, valid, n == 0);
+      store_row(t_acc, dst, 64, g ? P.scale : 1.0f, valid, n == 0);
+    } else {
+      uint16_t* dst = static_cast<uint16_t*>(P.dq) + out_row * 128;
+      store_row(tmem + lane_off + kColAcc0, dst, g * 64, P.scale, valid, n == 0);
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(c.bar(kAccEmpty));
+    __syncwarp();
+  }
+}
+
+template <int kPass>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_bf16_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tx1,
+                    const __grid_constant__ CUtensorMap ty0, const __grid_constant__ CUtensorMap ty1,
+                    const __grid_constant__ CUtensorMap tl, const BwdParams P) {
+  using C = Cfg<kPass>;
+  using B = Bars<kPass>;
+  static_assert(8 * B::kNum + 8 + 4 * kItemSlots <= 256, "barrier area");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t off_slot = C::kOffBar + 8 * B::kNum;
+  Ctl c{sbase + C::kOffBar, reinterpret_cast<volatile uint32_t*>(sgen + off_slot + 4), P.status};
+  volatile int32_t* slots = reinterpret_cast<volatile int32_t*>(sgen + off_slot + 8);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(c.bar(kFixFull), 1);
+    ptx::mbar_init(c.bar(kFixEmpty), 1);
+    ptx::mbar_init(c.bar(kAccFull), 1);
+    ptx::mbar_init(c.bar(kAccEmpty), 256);
+    ptx::mbar_init(c.bar(kDone), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(c.bar(kSFull + b), 1);
+      ptx::mbar_init(c.bar(kPFull + b), 128);
+    }
+    for (int s = 0; s < kItemSlots; ++s) {
+      ptx::mbar_init(c.bar(kItemFull + s), 1);
+      ptx::mbar_init(c.bar(kItemEmpty + s), kItemConsumers);
+    }
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(c.bar(kStFull + s), 1);
+      ptx::mbar_init(c.bar(B::kStEmpty + s), 1);
+    }
+    *c.abort = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tx0);
+    ptx::tma_prefetch_desc(&tx1);
+    ptx::tma_prefetch_desc(&ty0);
+    ptx::tma_prefetch_desc(&ty1);
+    if (kPass == 0) ptx::tma_prefetch_desc(&tl);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + off_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sgen + off_slot);
+
+  ProducerState ps{0u, 0u};
+  if (warp < 4) {
+    ptx::regs_release<kRegsOther>();
+    if (warp == 0) {
+      run_producer<kPass>(P, c, sbase, slots, &tx0, &tx1, &ty0, &ty1, &tl, ps);
+      __syncwarp();
+    } else if (warp == 1) {
+      run_mma<kPass>(P, c, sbase, slots, tmem);
+      ptx::mma_commit_warp(c.bar(kDone));
+      drain_bar(c, c.bar(kDone), 0);
+      __syncwarp();
+    }
+  } else {
+    ptx::regs_acquire<kRegsCompute>();
+    run_elementwise<kPass>(P, c, sgen, slots, tmem, (warp - 4) >> 2, warp & 3, lane);
+  }
+
+  if (warp == 0 && lane == 0 && *c.abort) {
+    // Let this CTA's own TMA loads land before its shared memory goes away.
+    for (uint32_t s = 0; s < (uint32_t)C::kStages; ++s) {
+      if (ps.str_issued > s) {
+        const uint32_t uses = (ps.str_issued - 1 - s) / C::kStages + 1;
+        drain_bar(c, c.bar(kStFull + (int)s), (uses - 1) & 1u);
+      }
+    }
+    if (ps.fix_issued > 0) drain_bar(c, c.bar(kFixFull), (ps.fix_issued - 1) & 1u);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [rows, 128] bf16 row-major; boxes of box_rows rows x 64 columns, 128-byte swizzle.
+bool encode_bf16(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128 * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [rows, 4] float32 ({lse2, D, 0, 0} per row); boxes of 64 rows, no swizzle.
+bool encode_lse(CUtensorMap* map, const void* base, int64_t rows) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {4, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {16};
+  const cuuint32_t box[2] = {4, 64};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kPass>
+cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUtensorMap& tx1, const CUtensorMap& ty0,
+                        const CUtensorMap& ty1, const CUtensorMap& tl, int grid, cudaStream_t stream,
+                        const char** why) {
+  using C = Cfg<kPass>;
+  cudaFuncAttributes attr;
+  cudaError_t e = cudaFuncGetAttributes(&attr, bwd_bf16_kernel<kPass>);
+  if (e != cudaSuccess) {
+    *why = "cudaFuncGetAttributes failed";
+    return e;
+  }
+  // setmaxnreg.inc waits until the registers exist: only launch when the split fits.
+  if ((uint32_t)attr.numRegs * kThreads < 128 * kRegsOther + 256 * kRegsCompute) {
+    *why = "kernel was built with fewer launch registers than its warpgroup split needs";
+    return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(bwd_bf16_kernel<kPass>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)C::kSmemBytes);
+  if (e != cudaSuccess) {
+    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
+  }
+  bwd_bf16_kernel<kPass><<<grid, kThreads, C::kSmemBytes, stream>>>(tx0, tx1, ty0, ty1, tl, prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) *why = "tensor-core backward launch failed";
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_bf16(int pass, const BwdParams& prm, const void* q, const void* k, const void* v,
+                            const void* dout, int grid, cudaStream_t stream, const char** why) {
+  CUtensorMap a, b, y0, y1, tl;
+  const int64_t rows_q = (int64_t)prm.batch * prm.heads_q * prm.seq;
+  const int64_t rows_kv = (int64_t)prm.batch * prm.heads_kv * prm.seq;
+  bool ok;
+  if (pass == 0)  // own tiles K, V (128 rows); streamed Q, dO (64 rows) and {lse2, D}
+    ok = encode_bf16(&a, k, rows_kv, kFixRows) && encode_bf16(&b, v, rows_kv, kFixRows) &&
+         encode_bf16(&y0, q, rows_q, kStreamRows) && encode_bf16(&y1, dout, rows_q, kStreamRows) &&
+         encode_lse(&tl, prm.lse2d, rows_q);
+  else            // own tiles Q, dO; streamed K, V
+    ok = encode_bf16(&a, q, rows_q, kFixRows) && encode_bf16(&b, dout, rows_q, kFixRows) &&
+         encode_bf16(&y0, k, rows_kv, kStreamRows) && encode_bf16(&y1, v, rows_kv, kStreamRows) &&
+         encode_lse(&tl, prm.lse2d, rows_q);
+  if (!ok) {
+    *why = "cuTensorMapEncodeTiled failed or is unavailable";
+    return cudaErrorInvalidValue;
+  }
+  return pass == 0 ? launch_pass<0>(prm, a, b, y0, y1, tl, grid, stream, why)
+                   : launch_pass<1>(prm, a, b, y0, y1, tl, grid, stream, why);
+}
+
+}  // namespace ra

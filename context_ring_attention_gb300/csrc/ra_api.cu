@@ -27,11 +27,14 @@ struct ra_plan_s {
   int n_qtiles, n_ktiles;
   std::vector<ra::WorkItem> items;       // whole forward: all N steps per item
   std::vector<ra::WorkItem> step_items;  // per-step lists, concatenated
+  std::vector<ra::WorkItem> bwd_items;   // backward: key tiles (dK, dV), then query tiles (dQ)
+  int64_t n_bwd_kv = 0;                  // how many of bwd_items are key tiles
   std::vector<int64_t> step_off;         // list of step t is [step_off[t], step_off[t+1])
   std::vector<int64_t> full, partial, skip;
   int device = -1;
   ra::WorkItem* d_items = nullptr;
   ra::WorkItem* d_step_items = nullptr;
+  ra::WorkItem* d_bwd_items = nullptr;
   uint32_t* d_status = nullptr;
   cudaEvent_t ev_entry = nullptr, ev_rot = nullptr, ev_step = nullptr;  // ra_ring_fwd ordering
   bool round_sync = false;  // forward kernel schedule (ra::use_round_sync)
@@ -115,6 +118,84 @@ std::vector<ra::WorkItem> schedule(const std::vector<Keyed>& list, int heads_q, 
   return out;
 }
 
+// Backward work lists.  dK/dV: one item per 128-row key tile (bh0 = b*Hkv + kv
+// head, shard r, row0, maxq = position of the tile's first key), costed by the
+// 64-row query tiles it meets over the ring (every query head of its group).
+// dQ: one item per 128-row query tile (bh0 = b*Hq + h, shard p, row0, maxq =
+// position of its last query), costed by the 64-row key tiles it meets.  Both in
+// the forward's order rule (longest first, key/value heads grouped).
+void build_bwd_schedule(ra_plan_s* pl) {
+  const ra_problem& pb = pl->prob;
+  const int N = pb.n_shards;
+  const int64_t s_n = pl->s_n;
+  const int G = pb.heads_q / pb.heads_kv;
+  const int n128 = (int)((s_n + 127) / 128), n64 = (int)((s_n + 63) / 64);
+  std::vector<Keyed> kv, qs;
+  int64_t seqno = 0;
+  for (int r = 0; r < N; ++r)
+    for (int kt = 0; kt < n128; ++kt)
+      for (int64_t b = 0; b < pb.batch; ++b)
+        for (int hk = 0; hk < pb.heads_kv; ++hk) {
+          ra::WorkItem w{};
+          w.bh0 = (int32_t)(b * pb.heads_kv + hk);
+          w.bh1 = -1;
+          w.shard = r;
+          w.row0 = kt * 128;
+          w.maxq = (int32_t)ra::pos_of(pb.layout, N, s_n, r, w.row0);
+          int cost = 0;
+          for (int t = 0; t < N; ++t) {
+            const int p = (r + t) % N;
+            int lo = 0;
+            if (pb.causal) {
+              const int64_t f = ra::first_ge(pb.layout, N, s_n, p, w.maxq);
+              lo = f >= s_n ? n64 : (int)(f / 64);
+            }
+            cost += (n64 - lo) * G;
+          }
+          w.cost = cost;
+          kv.push_back({w, seqno++});
+        }
+  for (int p = 0; p < N; ++p)
+    for (int qt = 0; qt < n128; ++qt)
+      for (int64_t b = 0; b < pb.batch; ++b)
+        for (int h = 0; h < pb.heads_q; ++h) {
+          ra::WorkItem w{};
+          w.bh0 = (int32_t)(b * pb.heads_q + h);
+          w.bh1 = -1;
+          w.shard = p;
+          w.row0 = qt * 128;
+          w.maxq = (int32_t)last_row_pos(pb, s_n, p, w.row0);
+          int cost = 0;
+          for (int t = 0; t < N; ++t) {
+            const int r = (p - t + N) % N;
+            if (!pb.causal) {
+              cost += n64;
+            } else {
+              const int64_t j = ra::last_le(pb.layout, N, s_n, r, w.maxq);
+              cost += j < 0 ? 0 : (int)(j / 64) + 1;
+            }
+          }
+          w.cost = cost;
+          qs.push_back({w, seqno++});
+        }
+  // schedule_key groups by key/value head from bh0 / heads_q: give the key-tile
+  // items a query-head index of their group so that they group the same way.
+  std::vector<Keyed> kv_keyed = kv;
+  for (Keyed& k : kv_keyed) {
+    const int64_t b = k.w.bh0 / pb.heads_kv, hk = k.w.bh0 % pb.heads_kv;
+    k.w.bh0 = (int32_t)(b * pb.heads_q + hk * G);
+  }
+  std::vector<ra::WorkItem> kv_sorted = schedule(kv_keyed, pb.heads_q, G);
+  for (ra::WorkItem& w : kv_sorted) {
+    const int64_t b = w.bh0 / pb.heads_q, hk = (w.bh0 % pb.heads_q) / G;
+    w.bh0 = (int32_t)(b * pb.heads_kv + hk);
+  }
+  const std::vector<ra::WorkItem> q_sorted = schedule(qs, pb.heads_q, G);
+  pl->bwd_items = kv_sorted;
+  pl->bwd_items.insert(pl->bwd_items.end(), q_sorted.begin(), q_sorted.end());
+  pl->n_bwd_kv = (int64_t)kv_sorted.size();
+}
+
 void build_schedule(ra_plan_s* pl) {
   const ra_problem& pb = pl->prob;
   const int N = pb.n_shards;
@@ -191,6 +272,8 @@ void build_schedule(ra_plan_s* pl) {
   for (const Keyed& k : list) max_cost = std::max<int64_t>(max_cost, k.w.cost);
   pl->round_sync = ra::use_round_sync(pb.seq, pb.head_dim, max_cost);
 
+  build_bwd_schedule(pl);
+
   // One list per ring step: the same items, costed by that step's key tiles alone.
   // Items with no causal key in the step stay in the list (they write the empty
   // partial: O_t = 0, LSE_t = -inf).
@@ -233,6 +316,12 @@ ra_status upload(ra_plan_s* pl) {
     e = cudaMalloc(&pl->d_step_items, pl->step_items.size() * sizeof(ra::WorkItem));
     if (e == cudaSuccess)
       e = cudaMemcpy(pl->d_step_items, pl->step_items.data(), pl->step_items.size() * sizeof(ra::WorkItem),
+                     cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess && !pl->bwd_items.empty()) {
+    e = cudaMalloc(&pl->d_bwd_items, pl->bwd_items.size() * sizeof(ra::WorkItem));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(pl->d_bwd_items, pl->bwd_items.data(), pl->bwd_items.size() * sizeof(ra::WorkItem),
                      cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_entry, cudaEventDisableTiming);
@@ -368,6 +457,7 @@ ra_status ra_plan_destroy(ra_plan_t plan) {
     if (cur != plan->device) cudaSetDevice(plan->device);
     cudaFree(plan->d_items);
     cudaFree(plan->d_step_items);
+    cudaFree(plan->d_bwd_items);
     cudaFree(plan->d_status);
     if (plan->ev_entry) cudaEventDestroy(plan->ev_entry);
     if (plan->ev_rot) cudaEventDestroy(plan->ev_rot);
@@ -551,6 +641,64 @@ ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* 
     if ((e = cudaEventRecord(plan->ev_step, st)) != cudaSuccess) return cuda_fail("event record");
   }
   return ra_merge_partials(N, rows, pb.head_dim, o_parts, lse_parts, o, pb.dtype, lse, st);
+}
+
+ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, float* scratch, void* stream) {
+  if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
+  const ra_problem& pb = plan->prob;
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, scratch};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return fail(RA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+  }
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t rows = pb.batch * (int64_t)pb.heads_q * pb.seq;
+  float4* lse2d = reinterpret_cast<float4*>(scratch);
+  cudaError_t e = ra::launch_bwd_prep(pb.dtype, rows, pb.head_dim, o, dout, lse, lse2d, st);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "backward preparation launch failed: %s", cudaGetErrorString(e));
+
+  ra::BwdParams prm{};
+  prm.batch = (int32_t)pb.batch;
+  prm.heads_q = pb.heads_q;
+  prm.heads_kv = pb.heads_kv;
+  prm.group = pb.heads_q / pb.heads_kv;
+  prm.head_dim = pb.head_dim;
+  prm.n_shards = pb.n_shards;
+  prm.layout = (int16_t)pb.layout;
+  prm.causal = (int16_t)pb.causal;
+  prm.seq = pb.seq;
+  prm.s_n = plan->s_n;
+  prm.scale = pb.scale;
+  prm.scale_log2 = pb.scale * 1.4426950408889634f;
+  prm.lse2d = lse2d;
+  prm.dq = dq;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.status = plan->d_status;
+  prm.item_counter = plan->d_status + 1;
+  if (pb.dtype != RA_DTYPE_BF16) {
+    e = ra::launch_bwd_f32(prm, static_cast<const float*>(q), static_cast<const float*>(k),
+                           static_cast<const float*>(v), static_cast<const float*>(dout), st);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "f32 backward launch failed: %s", cudaGetErrorString(e));
+    return ok();
+  }
+  const int sms = plan->sm_count > 0 ? plan->sm_count : 148;
+  for (int pass = 0; pass < 2; ++pass) {
+    const int64_t n = pass == 0 ? plan->n_bwd_kv : (int64_t)plan->bwd_items.size() - plan->n_bwd_kv;
+    prm.items = plan->d_bwd_items + (pass == 0 ? 0 : plan->n_bwd_kv);
+    prm.n_items = (int32_t)n;
+    if (n == 0) continue;
+    // each pass hands out work items from a counter that starts at zero
+    e = cudaMemsetAsync(prm.item_counter, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
+    const char* why = "";
+    e = ra::launch_bwd_bf16(pass, prm, q, k, v, dout, (int)std::min<int64_t>(n, sms), st, &why);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
+  }
+  return ok();
 }
 
 ra_status ra_sync_status(ra_plan_t plan, void* stream) {

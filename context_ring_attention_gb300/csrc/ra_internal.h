@@ -128,6 +128,30 @@ struct FwdParams {
 };
 static_assert(sizeof(FwdParams) <= 128, "FwdParams grew past 128 bytes");
 
+// Smallest local row i of shard p whose position is >= P (s_n when none): positions
+// rise with the local row, so the queries of shard p that see a key at position P
+// are exactly rows first_ge(p, P)..s_n-1.
+RA_HD int64_t first_ge(int layout, int n_shards, int64_t s_n, int p, int64_t P) {
+  return last_le(layout, n_shards, s_n, p, P - 1) + 1;
+}
+
+// Backward-pass kernels (dQ, dK, dV from dO, with the forward's LSE).
+struct BwdParams {
+  int32_t batch, heads_q, heads_kv, group, head_dim, n_shards;
+  int16_t layout, causal;
+  int32_t n_items;  // tensor-core kernels: work items of this pass
+  int64_t seq, s_n;
+  float scale;       // score scale
+  float scale_log2;  // scale * log2(e)
+  const float4* lse2d;  // [B*Hq*S] {LSE * log2(e), D = rowsum(dO * O), 0, 0}
+  void* dq;             // [B, Hq, S, d], plan dtype
+  void* dk;             // [B, Hkv, S, d]
+  void* dv;
+  const WorkItem* items;
+  uint32_t* status;
+  uint32_t* item_counter;
+};
+
 // Status bits written by kernels into the plan's status word.
 enum : uint32_t {
   kStatusTimeoutProducer = 1u << 0,
@@ -156,6 +180,13 @@ cudaError_t launch_layout_perm(int layout, int64_t seq, int n_shards, int invers
                                int64_t rows_outer, int row_bytes, const void* src, void* dst,
                                cudaStream_t stream);
 int fwd_bf16_smem_bytes();
+cudaError_t launch_bwd_prep(int dtype, int64_t rows, int d, const void* o, const void* dout, const float* lse,
+                            float4* out, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const BwdParams& prm, const float* q, const float* k, const float* v,
+                           const float* dout, cudaStream_t stream);
+// pass 0: dK and dV (items are key tiles); pass 1: dQ (items are query tiles).
+cudaError_t launch_bwd_bf16(int pass, const BwdParams& prm, const void* q, const void* k, const void* v,
+                            const void* dout, int grid, cudaStream_t stream, const char** why);
 
 // Sets the thread-local message returned by ra_last_error().
 void set_last_error(const char* msg);

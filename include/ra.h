@@ -35,9 +35,9 @@
  *   - Scores are s = scale * q.k with scale = 1/sqrt(d) unless given.
  *
  * Ownership: the caller owns every device buffer passed in.  A plan owns its
- * host tables, its device work tables (whole forward and one per ring step), its
- * device status word and three CUDA events; ra_fwd, ra_fwd_step, ra_ring_rotate,
- * ra_ring_fwd, ra_merge_partials and ra_layout_perm allocate nothing and are
+ * host tables, its device work tables (whole forward, one per ring step, backward),
+ * its device status word and three CUDA events; ra_fwd, ra_fwd_step, ra_ring_rotate,
+ * ra_ring_fwd, ra_bwd, ra_merge_partials and ra_layout_perm allocate nothing and are
  * asynchronous on the given stream (a cudaStream_t passed as void*; NULL = legacy
  * default).
  *
@@ -207,6 +207,35 @@ ra_status ra_ring_rotate(ra_plan_t plan, const void* k_src, const void* v_src, v
 ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, void* o,
                       float* lse, void* k_buf, void* v_buf, float* o_parts, float* lse_parts,
                       void* stream, void* comm_stream);
+
+/*
+ * ra_bwd -- gradients of the ring-attention forward (dQ, dK, dV from dO).
+ * The pages present ring attention as a way to train on long sequences (the
+ * activations of every layer are kept for the backward pass: "3.6 Distributed
+ * Training II", section "Ring Attention") but print no backward pass; this one
+ * differentiates the forward's definition O = softmax(scale * Q K^T + M) V:
+ *   P = exp(scale * Q K^T + M - LSE)   (recomputed from the forward's LSE)
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  D = rowsum(dO * O),
+ *   dQ = scale * dS K,  dK = scale * dS^T Q,
+ * with a key/value head's dK and dV summed over the query heads that read it.
+ * The work follows the ring: a query tile of shard p meets the key blocks of
+ * shards (p - t) mod N (as in the forward); a key block of shard r meets the
+ * queries of shard (r + t) mod N at step t, so its gradients gather where the
+ * block travels.
+ * q, k, v, o, dout (dO): as for ra_fwd (layout order, plan dtype); o and lse
+ *   are the forward's outputs for the same q, k, v.
+ * dq [B, Hq, S, d], dk and dv [B, Hkv, S, d]: outputs, plan dtype.
+ * scratch: caller-owned float32 device buffer of 4 * B * Hq * S floats (per query
+ *   row {LSE * log2(e), D, unused, unused}).
+ * Device pointers, 16-byte aligned.  Asynchronous on stream; allocates nothing.
+ * A device-side wait that runs out of budget is reported by ra_sync_status.
+ * Calls that share a plan must not overlap on the GPU.
+ * Errors: RA_ERR_INVALID_ARG (null/misaligned pointers), RA_ERR_NO_DEVICE,
+ * RA_ERR_CUDA.
+ */
+ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, const void* o,
+                 const float* lse, const void* dout, void* dq, void* dk, void* dv, float* scratch,
+                 void* stream);
 
 /*
  * ra_merge_partials -- exact combination of partial attention results.

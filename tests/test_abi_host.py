@@ -158,3 +158,16 @@ def test_plan_rejects_too_many_shards(lib):
     with pytest.raises(ra.RaError) as ei:
         ra.ra_plan(1, 65536, 1, 1, 128, 32768, "contiguous", False, "bf16")
     assert ei.value.status == 2
+
+
+def test_bwd_checks_arguments(lib):
+    plan = ra.ra_plan(1, 1024, 4, 2, 128, 4, "zigzag", True, "bf16")
+    a = 1 << 20
+    h = plan.handle
+    assert lib.ra_bwd(h, a, a, a, a, a, a, a, a, a, None, None) == 1     # null scratch
+    assert lib.ra_bwd(h, a, a, a, a, a, a, a, a, a + 4, a, None) == 1    # misaligned dv
+    assert lib.ra_bwd(None, a, a, a, a, a, a, a, a, a, a, None) == 1
+    pytest.importorskip("torch")
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.ra_bwd(h, a, a, a, a, a, a, a, a, a, a, None) == 5

@@ -1,0 +1,113 @@
+"""GPU parity of the backward pass (ra_bwd) against the float64 oracle.
+
+The oracle differentiates the forward's definition (pinned by finite differences
+in the oracle's own tests).  Both sides read the same bf16 (or f32) inputs; the
+kernels use the forward's own O and LSE, as a training step would.
+
+Tolerance for bf16 gradients, from the arithmetic.  P and dS enter the tensor-core
+products rounded to bf16 (relative error up to 2^-9 each), and the outputs are
+rounded to bf16 once more; everything else accumulates in fp32.  Elementwise
+relative errors then stay near 2^-9, but the gradients are sums with heavy
+cancellation (each row of dS sums to zero).  So the error is measured against
+the size of the whole tensor: relative RMS <= 1e-2 (about 5x the 2^-9 rounding
+of three bf16 factors), and max-abs <= 2e-2 times the tensor's largest
+magnitude.  float32 problems: max-abs 1e-4 times the largest magnitude, since
+the sums run over up to a few hundred fp32 terms.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import to64
+
+torch = pytest.importorskip("torch")
+ra = pytest.importorskip("context_ring_attention_gb300")
+from context_ring_attention_gb300 import workloads  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+BWD_REL_RMS = 1e-2
+BWD_MAX_REL = 2e-2
+F32_MAX_REL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ra.load_library()
+
+
+def _close(got, want, what, rel_rms=BWD_REL_RMS, max_rel=BWD_MAX_REL):
+    got, want = np.asarray(got, np.float64), np.asarray(want, np.float64)
+    assert np.isfinite(got).all(), f"{what}: non-finite"
+    scale = np.abs(want).max()
+    err = np.abs(got - want).max()
+    rr = np.sqrt(np.mean((got - want) ** 2)) / max(np.sqrt(np.mean(want ** 2)), 1e-30)
+    assert err <= max_rel * scale, f"{what}: max-abs {err:.3e} > {max_rel} x {scale:.3e}"
+    assert rr <= rel_rms, f"{what}: rel-RMS {rr:.3e} > {rel_rms}"
+    return err / scale, rr
+
+
+def _run(B, S, Hq, Hkv, n, layout, causal, seed, dtype="bf16", d=128, q_scale=1.0):
+    q, k, v = workloads.small_inputs(B, S, Hq, Hkv, d, seed=seed, device="cuda", dtype=dtype, q_scale=q_scale)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed + 1000)
+    do = torch.randn(q.shape, generator=g, device="cuda").to(q.dtype)
+    pos = oracle.layout_positions(layout, S, n)
+    pos_t = torch.from_numpy(pos).cuda()
+    ql, kl, vl, dol = (t.index_select(2, pos_t).contiguous() for t in (q, k, v, do))
+    plan = ra.ra_plan(B, S, Hq, Hkv, d, n, layout, causal, dtype)
+    o, lse = ra.ra_fwd(plan, ql, kl, vl)
+    dq, dk, dv = ra.ra_bwd(plan, ql, kl, vl, o, lse, dol)
+    ra.ra_sync_status(plan)
+    want = oracle.attention_backward(to64(ql), to64(kl), to64(vl), to64(dol), causal=causal, positions=pos)
+    return (dq, dk, dv), want
+
+
+SHAPES = [
+    # B, S, Hq, Hkv, N
+    (1, 1024, 4, 2, 2),    # 512 rows per shard
+    (1, 900, 4, 2, 3),     # 300 rows per shard: ragged 64- and 128-row tiles
+    (2, 640, 2, 2, 4),     # G = 1
+    (1, 768, 6, 2, 2),     # G = 3
+    (1, 256, 8, 1, 1),     # N = 1, G = 8
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("layout", oracle.LAYOUTS)
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_backward_matches_oracle(shape, layout, causal):
+    B, S, Hq, Hkv, n = shape
+    if layout == "zigzag" and S % (2 * n):
+        pytest.skip("zigzag needs 2N | S")
+    got, want = _run(B, S, Hq, Hkv, n, layout, causal, seed=sum(shape) + 5)
+    for name, g_, w_ in zip(("dQ", "dK", "dV"), got, want):
+        _close(to64(g_), w_, f"{name} {layout} causal={causal} {shape}")
+
+
+def test_bf16_backward_short_shards_and_large_logits():
+    # 40 rows per shard (every tile ragged); Q x4 (peaked probabilities)
+    for args in ((1, 320, 2, 1, 8, "zigzag", True, 41, 1.0), (1, 1024, 4, 2, 4, "contiguous", True, 42, 4.0)):
+        B, S, Hq, Hkv, n, layout, causal, seed, qs = args
+        got, want = _run(B, S, Hq, Hkv, n, layout, causal, seed=seed, q_scale=qs)
+        for name, g_, w_ in zip(("dQ", "dK", "dV"), got, want):
+            _close(to64(g_), w_, f"{name} {args}")
+
+
+def test_bf16_backward_deterministic():
+    got1, _ = _run(1, 2048, 8, 2, 4, "zigzag", True, seed=51)
+    got2, _ = _run(1, 2048, 8, 2, 4, "zigzag", True, seed=51)
+    for a, b in zip(got1, got2):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
+def test_f32_backward_matches_oracle(causal, layout):
+    # Module 23's example shape: (2, 4, 96, 32) in float32, 4 devices
+    got, want = _run(2, 96, 4, 4, 4, layout, causal, seed=61, dtype="f32", d=32)
+    for name, g_, w_ in zip(("dQ", "dK", "dV"), got, want):
+        _close(to64(g_), w_, f"f32 {name}", rel_rms=1e-5, max_rel=F32_MAX_REL)
