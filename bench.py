@@ -336,6 +336,10 @@ def run_ours(args, wl):
             "merge": merge_bandwidth(ra, torch, dev, stream),
         }
 
+    backward = None
+    if not args.no_bwd:
+        backward = backward_report(ra, torch, plan, (ql, kl, vl), (o_l, lse_l), stream, flops, pg)
+
     ring = None
     if args.path == "ring":
         ring = ring_driver_report(ra, torch, plan, N, (ql, kl, vl), (o_l, lse_l), (kbuf, vbuf),
@@ -369,6 +373,10 @@ def run_ours(args, wl):
         "algorithmic_flops_per_step": flops,
         "kernels": kernels,
     }
+    if backward is not None:
+        peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        backward["frac_of_sustained"] = backward["TFLOP/s"] / peak_s
+        line["backward"] = backward
     if ring is not None:
         line["ring_driver"] = ring
         line["config"]["path"] = "ring driver: per-step launches, K/V exchange on a second stream, merge"
@@ -423,6 +431,41 @@ def measured_traffic(workload):
         return int(rec["traffic_bytes_per_launch"])
     except (KeyError, ValueError, OSError):
         return None
+
+
+def backward_report(ra, torch, plan, qkv, out, stream, flops, pg):
+    """dQ, dK, dV of the timed forward's output for a random upstream gradient.
+
+    One untimed call, then one timed call (CUDA events around ra_bwd: the
+    preparation kernel and both tensor-core passes).  FLOPs are counted the usual
+    way for attention gradients, 2.5x the forward's (five matrix products per
+    (q, k) pair against two); the kernels execute 3.5x (scores and dP are
+    recomputed in both passes).
+    """
+    ql, kl, vl = qkv
+    o_l, lse_l = out
+    g = torch.Generator(device=ql.device)
+    g.manual_seed(4242)
+    dout = torch.randn(ql.shape, generator=g, device=ql.device).to(ql.dtype)
+    dq, dk, dv = torch.empty_like(ql), torch.empty_like(kl), torch.empty_like(vl)
+    scratch = torch.empty(tuple(ql.shape[:3]) + (4,), dtype=torch.float32, device=ql.device)
+    ra.ra_bwd(plan, ql, kl, vl, o_l, lse_l, dout, dq, dk, dv, scratch)
+    ra.ra_sync_status(plan)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg is not None:
+        pg.barrier()
+    torch.cuda.synchronize()
+    a.record(stream)
+    ra.ra_bwd(plan, ql, kl, vl, o_l, lse_l, dout, dq, dk, dv, scratch)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ra.ra_sync_status(plan)
+    ms = a.elapsed_time(b)
+    del dout, dq, dk, dv, scratch
+    return {"ms": ms, "TFLOP/s": 2.5 * flops / (ms * 1e-3) / 1e12,
+            "executed_TFLOP/s": 3.5 * flops / (ms * 1e-3) / 1e12,
+            "flops_convention": "2.5x forward (dV, dP, dQ, dK and the recomputed scores)",
+            "launches": 3}
 
 
 def ring_driver_report(ra, torch, plan, N, qkv, out, bufs, parts, stream, driver_ms, flops):
@@ -508,6 +551,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip the permute/merge bandwidth lines")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
     ap.add_argument("--path", default="fused", choices=["fused", "ring"],
                     help="fused: one ra_fwd launch per step; ring: the explicit ring driver "
                          "(per-step launches, K/V exchange on a second stream, merge)")
