@@ -448,7 +448,7 @@ def backward_report(ra, torch, plan, qkv, out, stream, flops, pg):
     g.manual_seed(4242)
     dout = torch.randn(ql.shape, generator=g, device=ql.device).to(ql.dtype)
     dq, dk, dv = torch.empty_like(ql), torch.empty_like(kl), torch.empty_like(vl)
-    scratch = torch.empty(tuple(ql.shape[:3]) + (4,), dtype=torch.float32, device=ql.device)
+    scratch = torch.empty(ra.ra_bwd_scratch_size(plan) // 4, dtype=torch.float32, device=ql.device)
     ra.ra_bwd(plan, ql, kl, vl, o_l, lse_l, dout, dq, dk, dv, scratch)
     ra.ra_sync_status(plan)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -21,7 +21,7 @@ __all__ = [
     "RaError", "Plan", "LAYOUTS",
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-    "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd",
+    "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -31,7 +31,7 @@ _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_
            4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd")
+            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -80,6 +80,7 @@ def load_library():
         "ra_ring_rotate": ([P, VP, VP, VP, VP, VP], I32),
         "ra_ring_fwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
         "ra_bwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
+        "ra_bwd_scratch_size": ([P, VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -345,7 +346,7 @@ def ra_bwd(plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scratch=None,
     """Gradients (dQ, dK, dV) of the forward for the upstream gradient ``dout``.
 
     ``o`` and ``lse`` are the forward's outputs for the same q, k, v; ``scratch``
-    (4 * B * Hq * S float32) is allocated here unless passed in.
+    (``ra_bwd_scratch_size`` bytes, float32) is allocated here unless passed in.
     """
     import torch
     pb = plan.problem
@@ -360,9 +361,18 @@ def ra_bwd(plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scratch=None,
     if dv is None:
         dv = torch.empty_like(v)
     if scratch is None:
-        scratch = torch.empty((B, Hq, S, 4), dtype=torch.float32, device=q.device)
+        scratch = torch.empty(ra_bwd_scratch_size(plan) // 4, dtype=torch.float32, device=q.device)
+    elif scratch.numel() * scratch.element_size() < ra_bwd_scratch_size(plan):
+        raise ValueError("scratch is smaller than ra_bwd_scratch_size(plan)")
     if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, S):
         raise ValueError("lse must be a contiguous float32 tensor of shape (B, Hq, S)")
     _check(load_library().ra_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(scratch), _stream(stream)))
     return dq, dk, dv
+
+
+def ra_bwd_scratch_size(plan):
+    """Bytes of the float32 scratch buffer ra_bwd needs for this plan."""
+    n = ctypes.c_int64()
+    _check(load_library().ra_bwd_scratch_size(plan.handle, ctypes.byref(n)))
+    return n.value

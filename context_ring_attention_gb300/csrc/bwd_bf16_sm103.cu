@@ -22,8 +22,8 @@
 // How (one persistent CTA per SM, 12 warps):
 //   warp 0     TMA producer: the item's two 128-row tiles (K, V in pass 0; Q, dO
 //              in pass 1) once, then 64-row tiles of the other two tensors (Q, dO
-//              and 64 {LSE*log2(e), D} rows in pass 0; K, V in pass 1) into a ring
-//              of stages.
+//              and the tile's 64 LSE*log2(e) and D values in pass 0; K, V in pass 1)
+//              into a ring of stages.
 //   warp 1     tcgen05 issuer (converged warp, one elected lane):
 //              per streamed tile two SS MMAs (M = 128, N = 64) give the scores and
 //              dP (pass 0 transposed: keys are the TMEM lanes), then TS MMAs
@@ -32,10 +32,12 @@
 //              the streamed tile, still in shared memory, as an MN-major operand.
 //   warps 4-7 / 8-11  elementwise: one thread per TMEM lane turns scores and dP
 //              into P and dS (bf16, written back into tensor memory), for the
-//              even / odd tiles of an item; at the end of an item they write the
+//              even / odd streamed tiles; at the end of an item they write the
 //              accumulators (pass 0: warps 4-7 dV, 8-11 dK; pass 1: half of dQ each).
-// TMEM: two tile buffers of 128 columns (scores 0-63, dP 64-127; P over 0-31 and
-// dS over 64-95 once computed), accumulators at 256-383 and 384-511.
+// TMEM: tile buffers of 128 columns (scores 0-63, dP 64-127; P over 0-31 and dS
+// over 64-95 once computed) -- two in pass 0, whose accumulators dV and dK take
+// columns 256-511, three in pass 1, whose accumulator dQ takes 384-511 -- so that
+// the MMAs of the next tiles run while the elementwise warps work on earlier ones.
 // Every wait is bounded (~1 s); on expiry the CTA records it in the status word,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -61,11 +63,12 @@ constexpr uint32_t kFixBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
 constexpr uint32_t kFixHalf = 128 * 64 * 2;       // its 128-byte swizzle column
 constexpr uint32_t kStrBytes = 64 * 128 * 2;      // one 64 x 128 bf16 tile
 constexpr uint32_t kStrHalf = 64 * 64 * 2;
-constexpr uint32_t kLseBytes = 64 * 16;           // 64 rows of float4 {lse2, D, 0, 0}
+constexpr uint32_t kLseBytes = 128 * 4;          // 64 lse2 values, then 64 D values
 
 template <int kPass>
 struct Cfg {
   static constexpr int kStages = kPass == 0 ? 4 : 5;
+  static constexpr int kBufs = kPass == 0 ? 2 : 3;  // score/dP buffers in tensor memory
   static constexpr uint32_t kStageBytes = kPass == 0 ? 2 * kStrBytes + 1024 : 2 * kStrBytes;
   static constexpr uint32_t kOffFix = 0;
   static constexpr uint32_t kOffStage = 2 * kFixBytes;
@@ -79,11 +82,11 @@ enum : int {
   kAccFull = 2,
   kAccEmpty = 3,
   kDone = 4,
-  kSFull = 5,       // 2
-  kPFull = 7,       // 2
-  kItemFull = 9,    // 4
-  kItemEmpty = 13,  // 4
-  kStFull = 17,     // kStages
+  kSFull = 5,       // 3 (one per buffer)
+  kPFull = 8,       // 3
+  kItemFull = 11,   // 4
+  kItemEmpty = 15,  // 4
+  kStFull = 19,     // kStages
 };
 template <int kPass>
 struct Bars {
@@ -94,8 +97,11 @@ constexpr int kItemSlots = 4;
 constexpr uint32_t kItemConsumers = 9;  // MMA warp + 8 elementwise warps
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColAcc0 = 256, kColAcc1 = 384;
-__device__ __forceinline__ uint32_t col_buf(int b) { return b ? 128u : 0u; }
+// pass 0: dV at 256, dK at 384; pass 1: dQ at 384
+template <int kPass>
+__device__ __forceinline__ uint32_t col_acc0() { return kPass == 0 ? 256u : 384u; }
+constexpr uint32_t kColAcc1 = 384;
+__device__ __forceinline__ uint32_t col_buf(uint32_t b) { return b * 128u; }
 constexpr uint32_t kColDP = 64;   // dP within a buffer; dS is written over its first 32 columns
 constexpr uint32_t kIdescSS = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescTS = ptx::idesc_bf16_f32(128, 128, false, true);
@@ -236,7 +242,7 @@ struct ProducerState {
 template <int kPass>
 __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
                              const CUtensorMap* tx0, const CUtensorMap* tx1, const CUtensorMap* ty0,
-                             const CUtensorMap* ty1, const CUtensorMap* tl, ProducerState& st) {
+                             const CUtensorMap* ty1, ProducerState& st) {
   using C = Cfg<kPass>;
   const int lane = threadIdx.x & 31;
   const uint64_t keep = ptx::l2_policy_evict_last();
@@ -290,7 +296,11 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
       ptx::tma_load_2d_warp_hint(dst + kStrHalf, ty0, c.bar(kStFull + (int)s), 64, y, keep);
       ptx::tma_load_2d_warp_hint(dst + kStrBytes, ty1, c.bar(kStFull + (int)s), 0, y, keep);
       ptx::tma_load_2d_warp_hint(dst + kStrBytes + kStrHalf, ty1, c.bar(kStFull + (int)s), 64, y, keep);
-      if (kPass == 0) ptx::tma_load_2d_warp(dst + 2 * kStrBytes, tl, c.bar(kStFull + (int)s), 0, y);
+      if (kPass == 0)  // the tile's 64 lse2 and 64 D values (one 512-byte block)
+        ptx::bulk_load_warp(dst + 2 * kStrBytes,
+                            P.lse2d + bwd_scalar_index((int64_t)b * P.heads_q + h_base + w.g, w.shard,
+                                                       (int64_t)w.it * kStreamRows, P.n_shards, P.n64),
+                            kLseBytes, c.bar(kStFull + (int)s));
       st.str_issued = ++s_it;
       walk_next<kPass>(w, P, it);
     }
@@ -327,57 +337,60 @@ __device__ __forceinline__ void issue_ts(uint32_t d, uint32_t a_tmem, uint32_t b
 template <int kPass>
 __device__ void run_mma(const BwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots, uint32_t tmem) {
   using C = Cfg<kPass>;
+  constexpr uint32_t NB = (uint32_t)C::kBufs;
   const int lane = threadIdx.x & 31;
   const uint32_t fix_lo = ptx::desc_lo(sbase + C::kOffFix, 16);
-  uint32_t s_it = 0, pj[2] = {0, 0};
+  uint32_t s_it = 0;  // streamed tiles so far (global tile index J of this CTA)
+  auto str_lo = [&](uint32_t J, uint32_t lbo) {
+    return ptx::desc_lo(sbase + C::kOffStage + (J % C::kStages) * C::kStageBytes, lbo);
+  };
+  auto wait_stage = [&](uint32_t J) {
+    return __all_sync(0xffffffffu, wait_bar(c, c.bar(kStFull + (int)(J % C::kStages)), (J / C::kStages) & 1u,
+                                            kStatusTimeoutMma));
+  };
+  // Scores and dP of tile J into buffer J % NB.
+  auto issue_tile_ss = [&](uint32_t J) {
+    if (!wait_stage(J)) return false;
+    issue_ss<kPass>(tmem, (int)(J % NB), fix_lo, str_lo(J, 16));
+    ptx::mma_commit_warp(c.bar(kSFull + (int)(J % NB)));
+    return true;
+  };
   for (uint32_t u = 0;; ++u) {
     const int idx = next_item(c, slots, u, lane);
     if (idx < 0) break;
     const WorkItem it = P.items[idx];
-    const int n = item_tiles<kPass>(P, it);
+    const uint32_t n = (uint32_t)item_tiles<kPass>(P, it);
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixFull), u & 1u, kStatusTimeoutMma))) return;
-    auto str_lo = [&](uint32_t i, uint32_t lbo) {
-      return ptx::desc_lo(sbase + C::kOffStage + ((s_it + i) % C::kStages) * C::kStageBytes, lbo);
-    };
-    auto wait_stage = [&](uint32_t i) {
-      return __all_sync(0xffffffffu, wait_bar(c, c.bar(kStFull + (int)((s_it + i) % C::kStages)),
-                                              ((s_it + i) / C::kStages) & 1u, kStatusTimeoutMma));
-    };
-    if (n > 0) {
-      if (!wait_stage(0)) return;
-      issue_ss<kPass>(tmem, 0, fix_lo, str_lo(0, 16));
-      ptx::mma_commit_warp(c.bar(kSFull + 0));
-    }
-    for (int i = 0; i < n; ++i) {
-      const int b = i & 1;
-      if (i + 1 < n) {  // next tile's scores and dP into the other buffer
-        if (!wait_stage((uint32_t)i + 1)) return;
-        issue_ss<kPass>(tmem, b ^ 1, fix_lo, str_lo((uint32_t)i + 1, 16));
-        ptx::mma_commit_warp(c.bar(kSFull + (b ^ 1)));
-      }
-      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kPFull + b), pj[b] & 1u, kStatusTimeoutMma))) return;
-      ++pj[b];
+    // Run NB - 1 tiles ahead: buffer (J + NB - 1) % NB was last used by tile J - 1,
+    // whose TS products are issued (the tensor pipe executes in issue order).
+    for (uint32_t a = 0; a + 1 < NB && a < n; ++a)
+      if (!issue_tile_ss(s_it + a)) return;
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t J = s_it + i;
+      if (i + NB - 1 < n && !issue_tile_ss(J + NB - 1)) return;
+      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kPFull + (int)(J % NB)), (J / NB) & 1u, kStatusTimeoutMma)))
+        return;
       if (i == 0 && u > 0 &&
           !__all_sync(0xffffffffu, wait_bar(c, c.bar(kAccEmpty), (u - 1) & 1u, kStatusTimeoutMma)))
         return;
       ptx::tc_fence_after();
-      // Streamed tile 0 (Q in pass 0, K in pass 1) and tile 1 (dO) as MN-major B.
-      const uint32_t y0 = str_lo((uint32_t)i, kStrHalf), y1 = y0 + (kStrBytes >> 4);
-      const uint32_t buf = tmem + col_buf(b);
+      // Streamed tile 0 (Q in pass 0, K in pass 1) and tile 1 (dO in pass 0) as MN-major B.
+      const uint32_t y0 = str_lo(J, kStrHalf), y1 = y0 + (kStrBytes >> 4);
+      const uint32_t buf = tmem + col_buf(J % NB);
       if (kPass == 0) {
-        issue_ts(tmem + kColAcc0, buf, y1, i > 0);           // dV += P^T dO
+        issue_ts(tmem + col_acc0<kPass>(), buf, y1, i > 0);  // dV += P^T dO
         issue_ts(tmem + kColAcc1, buf + kColDP, y0, i > 0);  // dK += dS^T Q
       } else {
-        issue_ts(tmem + kColAcc0, buf + kColDP, y0, i > 0);  // dQ += dS K
+        issue_ts(tmem + col_acc0<kPass>(), buf + kColDP, y0, i > 0);  // dQ += dS K
       }
-      ptx::mma_commit_warp(c.bar(kStFull + C::kStages + (int)((s_it + (uint32_t)i) % C::kStages)));
+      ptx::mma_commit_warp(c.bar(kStFull + C::kStages + (int)(J % C::kStages)));
     }
     if (n == 0 && u > 0 &&
         !__all_sync(0xffffffffu, wait_bar(c, c.bar(kAccEmpty), (u - 1) & 1u, kStatusTimeoutMma)))
       return;
     ptx::mma_commit_warp(c.bar(kAccFull));
     ptx::mma_commit_warp(c.bar(kFixEmpty));
-    s_it += (uint32_t)n;
+    s_it += n;
   }
 }
 
@@ -407,38 +420,51 @@ __device__ __forceinline__ void store_row(uint32_t t_acc, uint16_t* dst_row, int
   }
 }
 
+// P and dS for one pair of columns (live: both unmasked).
+__device__ __forceinline__ void p_ds_pair(float2 s2, float2 dp2, float2 l2, float2 d2, float2 sl2, bool live0,
+                                          bool live1, uint32_t& pw, uint32_t& dw) {
+  float2 x = ptx::fma2(s2, sl2, make_float2(-l2.x, -l2.y));
+  x.x = live0 ? ptx::ex2_approx(x.x) : 0.f;
+  x.y = live1 ? ptx::ex2_approx(x.y) : 0.f;
+  const float2 ds = ptx::mul2(x, ptx::add2(dp2, make_float2(-d2.x, -d2.y)));
+  pw = ptx::pack_bf16x2(x.x, x.y);
+  dw = ptx::pack_bf16x2(ds.x, ds.y);
+}
+
 template <int kPass>
 __device__ void run_elementwise(const BwdParams& P, const Ctl& c, const uint8_t* sgen, volatile int32_t* slots,
                                 uint32_t tmem, int g, int wq, int lane) {
   using C = Cfg<kPass>;
+  constexpr uint32_t NB = (uint32_t)C::kBufs;
   const int row = wq * 32 + lane;  // TMEM lane: key row (pass 0) or query row (pass 1)
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const int N = P.n_shards;
-  const float sl2 = P.scale_log2;
-  uint32_t s_it = 0, sj = 0;
+  const float2 sl2 = make_float2(P.scale_log2, P.scale_log2);
+  uint32_t s_it = 0;
   for (uint32_t u = 0;; ++u) {
     const int idx = next_item(c, slots, u, lane);
     if (idx < 0) break;
     const WorkItem it = P.items[idx];
-    const int n = item_tiles<kPass>(P, it);
+    const uint32_t n = (uint32_t)item_tiles<kPass>(P, it);
     const int64_t i_own = (int64_t)it.row0 + row;  // local row of the item's own tile
     const bool valid = i_own < P.s_n;
     const int64_t my_pos = pos_of(P.layout, N, P.s_n, it.shard, valid ? i_own : P.s_n - 1);
     const int64_t out_row = (int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + i_own;
-    float2 own = make_float2(0.f, 0.f);  // pass 1: this query row's {lse2, D}
+    float2 own_l = make_float2(0.f, 0.f), own_d = make_float2(0.f, 0.f);  // pass 1: this row's lse2, D
     if (kPass == 1 && valid) {
-      const float4 t4 = P.lse2d[out_row];
-      own = make_float2(t4.x, t4.y);
+      const int64_t li = bwd_scalar_index(it.bh0, it.shard, i_own, N, P.n64);
+      own_l = make_float2(P.lse2d[li], P.lse2d[li]);
+      own_d = make_float2(P.lse2d[li + 64], P.lse2d[li + 64]);
     }
 
     Walk w;
     walk_begin<kPass>(w, P, it);
-    for (int i = 0; i < n; ++i) {
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t J = s_it + i;
       const int64_t tile_lo = (int64_t)w.it * kStreamRows;  // first local row of the streamed tile
       const int shard = w.shard;
-      const uint32_t stage = (s_it + (uint32_t)i) % C::kStages;
       walk_next<kPass>(w, P, it);
-      if ((i & 1) != g) continue;
+      if ((int)(J & 1u) != g) continue;
       // Columns [c_lo, c_hi) of this tile are live for this row.
       int c_lo = 0;
       const int64_t left = P.s_n - tile_lo;
@@ -453,40 +479,47 @@ __device__ void run_elementwise(const BwdParams& P, const Ctl& c, const uint8_t*
           c_hi = lim < c_hi ? lim : c_hi;
         }
       }
-      const bool ok = wait_bar(c, c.bar(kSFull + g), sj & 1u, kStatusTimeoutSoftmax);
-      ++sj;
+      const bool ok = wait_bar(c, c.bar(kSFull + (int)(J % NB)), (J / NB) & 1u, kStatusTimeoutSoftmax);
       if (!__all_sync(0xffffffffu, ok)) return;
       ptx::tc_fence_after();
-      const uint32_t tb = tmem + lane_off + col_buf(g);
-      uint32_t raw[128];  // scores in 0-63, dP in 64-127
-      ptx::tmem_ld128(tb, raw);
-      // pass 0: the tile's queries' {lse2, D}, streamed with it (float4 rows)
-      const float4* lse_tile =
-          reinterpret_cast<const float4*>(sgen + C::kOffStage + stage * C::kStageBytes + 2 * kStrBytes);
+      const uint32_t tb = tmem + lane_off + col_buf(J % NB);
+      // pass 0: the tile's 64 lse2 values, then its 64 D values, in shared memory
+      const float4* l4 =
+          reinterpret_cast<const float4*>(sgen + C::kOffStage + (J % C::kStages) * C::kStageBytes + 2 * kStrBytes);
       uint32_t pw[32], dw[32];
+      const bool full = __all_sync(0xffffffffu, c_lo == 0 && c_hi == kStreamRows);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float pv[2], dsv[2];
+      for (int half = 0; half < 2; ++half) {  // columns 32*half .. 32*half + 31
+        uint32_t raw[64];                       // scores in 0-31, dP in 32-63
+        ptx::tmem_ld32x2(tb + 32u * half, tb + kColDP + 32u * half, raw);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int cc = 2 * e + h;
-          const float2 ld = kPass == 0 ? *reinterpret_cast<const float2*>(lse_tile + cc) : own;
-          const float sc = __uint_as_float(raw[cc]);
-          const float dp = __uint_as_float(raw[64 + cc]);
-          const bool live = cc >= c_lo && cc < c_hi;
-          const float pr = live ? ptx::ex2_approx(fmaf(sc, sl2, -ld.x)) : 0.f;
-          pv[h] = pr;
-          dsv[h] = pr * (dp - ld.y);
+        for (int q = 0; q < 8; ++q) {  // columns c0 .. c0+3 of the tile
+          const int c0 = 32 * half + 4 * q;
+          float4 L, D;
+          if (kPass == 0) {
+            L = l4[c0 / 4];
+            D = l4[16 + c0 / 4];
+          } else {
+            L = make_float4(own_l.x, own_l.x, own_l.x, own_l.x);
+            D = make_float4(own_d.x, own_d.x, own_d.x, own_d.x);
+          }
+          const bool a0 = full || (c0 >= c_lo && c0 < c_hi), a1 = full || (c0 + 1 >= c_lo && c0 + 1 < c_hi);
+          const bool b0 = full || (c0 + 2 >= c_lo && c0 + 2 < c_hi), b1 = full || (c0 + 3 >= c_lo && c0 + 3 < c_hi);
+          const int r0 = 4 * q;
+          p_ds_pair(make_float2(__uint_as_float(raw[r0]), __uint_as_float(raw[r0 + 1])),
+                    make_float2(__uint_as_float(raw[32 + r0]), __uint_as_float(raw[32 + r0 + 1])),
+                    make_float2(L.x, L.y), make_float2(D.x, D.y), sl2, a0, a1, pw[c0 / 2], dw[c0 / 2]);
+          p_ds_pair(make_float2(__uint_as_float(raw[r0 + 2]), __uint_as_float(raw[r0 + 3])),
+                    make_float2(__uint_as_float(raw[32 + r0 + 2]), __uint_as_float(raw[32 + r0 + 3])),
+                    make_float2(L.z, L.w), make_float2(D.z, D.w), sl2, b0, b1, pw[c0 / 2 + 1], dw[c0 / 2 + 1]);
         }
-        pw[e] = ptx::pack_bf16x2(pv[0], pv[1]);
-        dw[e] = ptx::pack_bf16x2(dsv[0], dsv[1]);
       }
       if (kPass == 0) ptx::tmem_st32(tb, pw);  // P^T for dV (pass 1 needs only dS)
       ptx::tmem_st32(tb + kColDP, dw);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(c.bar(kPFull + g));
+      ptx::mbar_arrive(c.bar(kPFull + (int)(J % NB)));
     }
-    s_it += (uint32_t)n;
+    s_it += n;
 
     // Item done: write the accumulators (pass 0: dV by warps 4-7, dK by 8-11;
     // pass 1: dQ columns 0-63 by warps 4-7, 64-127 by 8-11).
@@ -495,12 +528,12 @@ __device__ void run_elementwise(const BwdParams& P, const Ctl& c, const uint8_t*
     ptx::tc_fence_after();
     if (kPass == 0) {
       uint16_t* dst = static_cast<uint16_t*>(g ? P.dk : P.dv) + out_row * 128;
-      const uint32_t t_acc = tmem + lane_off + (g ? kColAcc1 : kColAcc0);
+      const uint32_t t_acc = tmem + lane_off + (g ? kColAcc1 : col_acc0<kPass>());
       store_row(t_acc, dst, 0, g ? P.scale : 1.0f, valid, n == 0);
       store_row(t_acc, dst, 64, g ? P.scale : 1.0f, valid, n == 0);
     } else {
       uint16_t* dst = static_cast<uint16_t*>(P.dq) + out_row * 128;
-      store_row(tmem + lane_off + kColAcc0, dst, g * 64, P.scale, valid, n == 0);
+      store_row(tmem + lane_off + col_acc0<kPass>(), dst, g * 64, P.scale, valid, n == 0);
     }
     ptx::tc_fence_before();
     ptx::mbar_arrive(c.bar(kAccEmpty));
@@ -512,7 +545,7 @@ template <int kPass>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_bf16_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tx1,
                     const __grid_constant__ CUtensorMap ty0, const __grid_constant__ CUtensorMap ty1,
-                    const __grid_constant__ CUtensorMap tl, const BwdParams P) {
+                    const BwdParams P) {
   using C = Cfg<kPass>;
   using B = Bars<kPass>;
   static_assert(8 * B::kNum + 8 + 4 * kItemSlots <= 256, "barrier area");
@@ -531,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(c.bar(kAccFull), 1);
     ptx::mbar_init(c.bar(kAccEmpty), 256);
     ptx::mbar_init(c.bar(kDone), 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::kBufs; ++b) {
       ptx::mbar_init(c.bar(kSFull + b), 1);
       ptx::mbar_init(c.bar(kPFull + b), 128);
     }
@@ -551,7 +584,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tma_prefetch_desc(&tx1);
     ptx::tma_prefetch_desc(&ty0);
     ptx::tma_prefetch_desc(&ty1);
-    if (kPass == 0) ptx::tma_prefetch_desc(&tl);
   }
   if (warp == 1) {
     ptx::tmem_alloc(sbase + off_slot, kTmemCols);
@@ -566,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     ptx::regs_release<kRegsOther>();
     if (warp == 0) {
-      run_producer<kPass>(P, c, sbase, slots, &tx0, &tx1, &ty0, &ty1, &tl, ps);
+      run_producer<kPass>(P, c, sbase, slots, &tx0, &tx1, &ty0, &ty1, ps);
       __syncwarp();
     } else if (warp == 1) {
       run_mma<kPass>(P, c, sbase, slots, tmem);
@@ -629,23 +661,9 @@ bool encode_bf16(CUtensorMap* map, const void* base, int64_t rows, uint32_t box_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [rows, 4] float32 ({lse2, D, 0, 0} per row); boxes of 64 rows, no swizzle.
-bool encode_lse(CUtensorMap* map, const void* base, int64_t rows) {
-  EncodeTiledFn enc = get_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {4, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {16};
-  const cuuint32_t box[2] = {4, 64};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int kPass>
 cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUtensorMap& tx1, const CUtensorMap& ty0,
-                        const CUtensorMap& ty1, const CUtensorMap& tl, int grid, cudaStream_t stream,
-                        const char** why) {
+                        const CUtensorMap& ty1, int grid, cudaStream_t stream, const char** why) {
   using C = Cfg<kPass>;
   cudaFuncAttributes attr;
   cudaError_t e = cudaFuncGetAttributes(&attr, bwd_bf16_kernel<kPass>);
@@ -664,7 +682,7 @@ cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUte
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  bwd_bf16_kernel<kPass><<<grid, kThreads, C::kSmemBytes, stream>>>(tx0, tx1, ty0, ty1, tl, prm);
+  bwd_bf16_kernel<kPass><<<grid, kThreads, C::kSmemBytes, stream>>>(tx0, tx1, ty0, ty1, prm);
   e = cudaGetLastError();
   if (e != cudaSuccess) *why = "tensor-core backward launch failed";
   return e;
@@ -674,24 +692,22 @@ cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUte
 
 cudaError_t launch_bwd_bf16(int pass, const BwdParams& prm, const void* q, const void* k, const void* v,
                             const void* dout, int grid, cudaStream_t stream, const char** why) {
-  CUtensorMap a, b, y0, y1, tl;
+  CUtensorMap a, b, y0, y1;
   const int64_t rows_q = (int64_t)prm.batch * prm.heads_q * prm.seq;
   const int64_t rows_kv = (int64_t)prm.batch * prm.heads_kv * prm.seq;
   bool ok;
   if (pass == 0)  // own tiles K, V (128 rows); streamed Q, dO (64 rows) and {lse2, D}
     ok = encode_bf16(&a, k, rows_kv, kFixRows) && encode_bf16(&b, v, rows_kv, kFixRows) &&
-         encode_bf16(&y0, q, rows_q, kStreamRows) && encode_bf16(&y1, dout, rows_q, kStreamRows) &&
-         encode_lse(&tl, prm.lse2d, rows_q);
+         encode_bf16(&y0, q, rows_q, kStreamRows) && encode_bf16(&y1, dout, rows_q, kStreamRows);
   else            // own tiles Q, dO; streamed K, V
     ok = encode_bf16(&a, q, rows_q, kFixRows) && encode_bf16(&b, dout, rows_q, kFixRows) &&
-         encode_bf16(&y0, k, rows_kv, kStreamRows) && encode_bf16(&y1, v, rows_kv, kStreamRows) &&
-         encode_lse(&tl, prm.lse2d, rows_q);
+         encode_bf16(&y0, k, rows_kv, kStreamRows) && encode_bf16(&y1, v, rows_kv, kStreamRows);
   if (!ok) {
     *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
-  return pass == 0 ? launch_pass<0>(prm, a, b, y0, y1, tl, grid, stream, why)
-                   : launch_pass<1>(prm, a, b, y0, y1, tl, grid, stream, why);
+  return pass == 0 ? launch_pass<0>(prm, a, b, y0, y1, grid, stream, why)
+                   : launch_pass<1>(prm, a, b, y0, y1, grid, stream, why);
 }
 
 }  // namespace ra

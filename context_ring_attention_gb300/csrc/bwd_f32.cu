@@ -48,7 +48,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     dos[warp][c] = dout[grow * d + c];
   }
   __syncwarp();
-  const float4 ld = P.lse2d[grow];
+  const int64_t li = bwd_scalar_index(bh, p, i, N, P.n64);
+  const float2 ld = make_float2(P.lse2d[li], P.lse2d[li + 64]);
   float acc[kMaxD / 32];
 #pragma unroll
   for (int x = 0; x < kMaxD / 32; ++x) acc[x] = 0.f;
@@ -116,7 +117,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         float pi = 0.f, ds = 0.f;
         if (i < P.s_n) {
           const int64_t row = qrow0 + i;
-          const float4 ld = P.lse2d[row];
+          const int64_t li = bwd_scalar_index((int64_t)b * P.heads_q + (int64_t)hk * P.group + g, p, i, N, P.n64);
+          const float2 ld = make_float2(P.lse2d[li], P.lse2d[li + 64]);
           pi = exp2f(fmaf(dot_row(q + row * d, ks[warp], d), P.scale_log2, -ld.x));
           ds = pi * (dot_row(dout + row * d, vs[warp], d) - ld.y);
         }

@@ -643,6 +643,14 @@ ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* 
   return ra_merge_partials(N, rows, pb.head_dim, o_parts, lse_parts, o, pb.dtype, lse, st);
 }
 
+ra_status ra_bwd_scratch_size(ra_plan_t plan, int64_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return fail(RA_ERR_INVALID_ARG, "null argument");
+  const ra_problem& pb = plan->prob;
+  const int64_t n64 = (plan->s_n + 63) / 64;
+  *bytes = pb.batch * (int64_t)pb.heads_q * pb.n_shards * n64 * 128 * (int64_t)sizeof(float);
+  return ok();
+}
+
 ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, const void* o, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv, float* scratch, void* stream) {
   if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
@@ -655,9 +663,9 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
   ra_status s = check_device(plan);
   if (s != RA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int64_t rows = pb.batch * (int64_t)pb.heads_q * pb.seq;
-  float4* lse2d = reinterpret_cast<float4*>(scratch);
-  cudaError_t e = ra::launch_bwd_prep(pb.dtype, rows, pb.head_dim, o, dout, lse, lse2d, st);
+  const int64_t n64 = (plan->s_n + 63) / 64;
+  cudaError_t e = ra::launch_bwd_prep(pb.dtype, pb.batch * (int64_t)pb.heads_q, pb.seq, pb.n_shards, pb.head_dim, o,
+                                      dout, lse, scratch, st);
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "backward preparation launch failed: %s", cudaGetErrorString(e));
 
   ra::BwdParams prm{};
@@ -673,7 +681,8 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
   prm.s_n = plan->s_n;
   prm.scale = pb.scale;
   prm.scale_log2 = pb.scale * 1.4426950408889634f;
-  prm.lse2d = lse2d;
+  prm.lse2d = scratch;
+  prm.n64 = n64;
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;

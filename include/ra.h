@@ -225,8 +225,8 @@ ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* 
  * q, k, v, o, dout (dO): as for ra_fwd (layout order, plan dtype); o and lse
  *   are the forward's outputs for the same q, k, v.
  * dq [B, Hq, S, d], dk and dv [B, Hkv, S, d]: outputs, plan dtype.
- * scratch: caller-owned float32 device buffer of 4 * B * Hq * S floats (per query
- *   row {LSE * log2(e), D, unused, unused}).
+ * scratch: caller-owned float32 device buffer of ra_bwd_scratch_size bytes (per
+ *   query row LSE * log2(e) and D, in blocks of 64 rows of one shard).
  * Device pointers, 16-byte aligned.  Asynchronous on stream; allocates nothing.
  * A device-side wait that runs out of budget is reported by ra_sync_status.
  * Calls that share a plan must not overlap on the GPU.
@@ -236,6 +236,13 @@ ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* 
 ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, const void* o,
                  const float* lse, const void* dout, void* dq, void* dk, void* dv, float* scratch,
                  void* stream);
+
+/*
+ * ra_bwd_scratch_size -- bytes of the scratch buffer ra_bwd needs for this plan:
+ * 512 bytes per 64-row block of every (batch, query head, shard), about
+ * 8 * B * Hq * S bytes.  Host only.  Errors: RA_ERR_INVALID_ARG (null arguments).
+ */
+ra_status ra_bwd_scratch_size(ra_plan_t plan, int64_t* bytes);
 
 /*
  * ra_merge_partials -- exact combination of partial attention results.

@@ -171,3 +171,10 @@ def test_bwd_checks_arguments(lib):
     import torch
     if not torch.cuda.is_available():
         assert lib.ra_bwd(h, a, a, a, a, a, a, a, a, a, a, None) == 5
+
+
+def test_bwd_scratch_size(lib):
+    # 64-row blocks of every (batch, query head, shard), 128 floats each
+    plan = ra.ra_plan(2, 900, 4, 2, 128, 3, "contiguous", True, "bf16")
+    assert ra.ra_bwd_scratch_size(plan) == 2 * 4 * 3 * 5 * 128 * 4   # 300 rows per shard -> 5 blocks
+    assert lib.ra_bwd_scratch_size(None, None) == 1
