@@ -233,6 +233,32 @@ __device__ __forceinline__ int next_item(const Ctl& c, volatile int32_t* slots, 
   return idx;
 }
 
+// Producer-side grid barrier for round-synchronised schedules: wait (bounded)
+// until the shared counter reaches `need`.
+__device__ __forceinline__ bool barrier_wait(const Ctl& c, const uint32_t* counter, uint32_t need, int lane) {
+  int ok = 1;
+  if (lane == 0) {
+    const volatile uint32_t* ctr = counter;
+    const uint64_t t0 = ptx::global_timer_ns();
+    for (uint32_t it = 0; *ctr < need; ++it) {
+      __nanosleep(128);
+      if ((it & 63u) == 63u) {
+        if (*c.abort) {
+          ok = 0;
+          break;
+        }
+        if (ptx::global_timer_ns() - t0 > kWaitBudgetNs) {
+          *c.abort = 1u;
+          atomicOr(c.status, kStatusTimeoutProducer);
+          ok = 0;
+          break;
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // ---------------------------------------------------------------- producer --
 struct ProducerState {
   uint32_t str_issued;  // streamed tiles issued
@@ -251,10 +277,18 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
     const uint32_t slot = u % kItemSlots, use = u / kItemSlots;
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kItemEmpty + (int)slot), (use & 1u) ^ 1u, kStatusTimeoutProducer)))
       break;
-    int idx = 0;
-    if (lane == 0) idx = (int)atomicAdd(P.item_counter, 1u);
-    idx = __shfl_sync(0xffffffffu, idx, 0);
-    if (idx >= P.n_items) idx = -1;
+    int idx;
+    if (P.round_sync) {
+      // Round u: item u*grid + b, once every CTA has issued the loads of round u-1.
+      idx = (int)(u * gridDim.x + blockIdx.x);
+      if (idx >= P.n_items) idx = -1;
+      if (idx >= 0 && u > 0 && !barrier_wait(c, P.item_counter, u * gridDim.x, lane)) idx = -1;
+    } else {
+      idx = 0;
+      if (lane == 0) idx = (int)atomicAdd(P.item_counter, 1u);
+      idx = __shfl_sync(0xffffffffu, idx, 0);
+      if (idx >= P.n_items) idx = -1;
+    }
     if (lane == 0) slots[slot] = idx;
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
@@ -305,6 +339,10 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
       walk_next<kPass>(w, P, it);
     }
     if (!ok) break;
+    if (P.round_sync) {
+      if (lane == 0) atomicAdd(P.item_counter, 1u);  // this CTA has issued its round
+      __syncwarp();
+    }
   }
 }
 
@@ -682,8 +720,24 @@ cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUte
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  bwd_bf16_kernel<kPass><<<grid, kThreads, C::kSmemBytes, stream>>>(tx0, tx1, ty0, ty1, prm);
-  e = cudaGetLastError();
+  if (prm.round_sync) {
+    // The rounds wait on each other: a cooperative launch guarantees co-residency.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute coop[1];
+    coop[0].id = cudaLaunchAttributeCooperative;
+    coop[0].val.cooperative = 1;
+    cfg.attrs = coop;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_bf16_kernel<kPass>, tx0, tx1, ty0, ty1, prm);
+    if (e == cudaSuccess) e = cudaGetLastError();
+  } else {
+    bwd_bf16_kernel<kPass><<<grid, kThreads, C::kSmemBytes, stream>>>(tx0, tx1, ty0, ty1, prm);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) *why = "tensor-core backward launch failed";
   return e;
 }

@@ -29,6 +29,7 @@ struct ra_plan_s {
   std::vector<ra::WorkItem> step_items;  // per-step lists, concatenated
   std::vector<ra::WorkItem> bwd_items;   // backward: key tiles (dK, dV), then query tiles (dQ)
   int64_t n_bwd_kv = 0;                  // how many of bwd_items are key tiles
+  bool bwd_round_sync[2] = {false, false};  // per backward pass (ra::use_round_sync)
   std::vector<int64_t> step_off;         // list of step t is [step_off[t], step_off[t+1])
   std::vector<int64_t> full, partial, skip;
   int device = -1;
@@ -191,6 +192,13 @@ void build_bwd_schedule(ra_plan_s* pl) {
     w.bh0 = (int32_t)(b * pb.heads_kv + hk);
   }
   const std::vector<ra::WorkItem> q_sorted = schedule(qs, pb.heads_q, G);
+  // Round sync when the streamed data of a head exceeds L2's reach and the longest
+  // item (in 64-row tiles, counted as half of a 128-row tile) stays short.
+  int64_t max_kv = 0, max_q = 0;
+  for (const Keyed& k : kv) max_kv = std::max<int64_t>(max_kv, k.w.cost);
+  for (const Keyed& k : qs) max_q = std::max<int64_t>(max_q, k.w.cost);
+  pl->bwd_round_sync[0] = ra::use_round_sync(pb.seq, pb.head_dim, max_kv / 2);
+  pl->bwd_round_sync[1] = ra::use_round_sync(pb.seq, pb.head_dim, max_q / 2);
   pl->bwd_items = kv_sorted;
   pl->bwd_items.insert(pl->bwd_items.end(), q_sorted.begin(), q_sorted.end());
   pl->n_bwd_kv = (int64_t)kv_sorted.size();
@@ -704,7 +712,13 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
     e = cudaMemsetAsync(prm.item_counter, 0, sizeof(uint32_t), st);
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "counter reset: %s", cudaGetErrorString(e));
     const char* why = "";
+    prm.round_sync = plan->bwd_round_sync[pass] ? 1 : 0;
     e = ra::launch_bwd_bf16(pass, prm, q, k, v, dout, (int)std::min<int64_t>(n, sms), st, &why);
+    if (e == cudaErrorCooperativeLaunchTooLarge) {  // not every CTA resident: dynamic schedule
+      cudaGetLastError();
+      prm.round_sync = 0;
+      e = ra::launch_bwd_bf16(pass, prm, q, k, v, dout, (int)std::min<int64_t>(n, sms), st, &why);
+    }
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   }
   return ok();

@@ -154,6 +154,7 @@ struct BwdParams {
   float scale_log2;  // scale * log2(e)
   const float* lse2d;   // per query row lse2 and D, in 64-row blocks (bwd_scalar_index)
   int64_t n64;          // 64-row blocks per shard
+  int32_t round_sync;   // hand out items in synchronised rounds (as FwdParams::round_sync)
   void* dq;             // [B, Hq, S, d], plan dtype
   void* dk;             // [B, Hkv, S, d]
   void* dv;
