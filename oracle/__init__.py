@@ -25,6 +25,8 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
                             zigzag's exact balance (the reading of "paired up
                             block-by-block").
 ``causal_pair_counts``      the same printed counts (golden fixture).
+``to_natural``              inverts the layout map (round trips for every layout; the contiguous
+                            layout is the identity).
 ``full_attention``          scipy.special.softmax / logsumexp on small cases; closed forms
                             (one key, identical keys, causal row 0); row sums of 1;
                             GQA head mapping against per-head single-head calls.
@@ -50,7 +52,7 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
 No function here is "parity unpinned".
 """
 
-from .layouts import CONTIGUOUS, STRIPED, ZIGZAG, LAYOUTS, layout_positions, causal_pair_counts
+from .layouts import CONTIGUOUS, STRIPED, ZIGZAG, LAYOUTS, layout_positions, causal_pair_counts, to_natural
 from .attention import attention_rows, full_attention, full_attention_rows
 from .ring import ring_sim, ring_partials, pass_blocks, held_blocks
 from .merge import merge_partials
@@ -59,7 +61,7 @@ from .tiles import tile_counts, tile_classes_bruteforce
 
 __all__ = [
     "CONTIGUOUS", "STRIPED", "ZIGZAG", "LAYOUTS",
-    "layout_positions", "causal_pair_counts",
+    "layout_positions", "causal_pair_counts", "to_natural",
     "full_attention", "full_attention_rows", "attention_rows",
     "ring_sim", "ring_partials", "pass_blocks", "held_blocks", "merge_partials",
     "attention_backward", "ring_backward",

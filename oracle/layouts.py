@@ -72,3 +72,16 @@ def causal_pair_counts(n_shards, block_size, layout):
         allowed = all_keys[None, :] <= q[:, None]
         work.append(int(allowed.sum()))
     return {"work": work, "imbalance": max(work) / min(work), "total": sum(work)}
+
+
+def to_natural(x, positions):
+    """Rows in layout order -> natural order along axis -2: out[..., pos[j], :] = x[..., j, :].
+
+    What the all-gather variant of context parallelism hands every device: the K/V
+    blocks of all shards, each row at its token position.
+    """
+    x = np.asarray(x)
+    pos = np.asarray(positions, np.int64)
+    out = np.empty_like(x)
+    out[..., pos, :] = x
+    return out

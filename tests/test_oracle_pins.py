@@ -432,3 +432,15 @@ def test_ring_backward_equals_attention_backward(layout, causal):
     got = oracle.ring_backward(q, k, v, do, o, lse, n, positions=pos, causal=causal)
     for g, w in zip(got, want):
         np.testing.assert_allclose(g, w, atol=1e-12)
+
+
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+def test_to_natural_inverts_the_layout(layout):
+    S, n = 48, 4
+    x = _rand((2, 3, S, 5), 100)
+    pos = layout_positions(layout, S, n)
+    np.testing.assert_array_equal(oracle.to_natural(x[..., pos, :], pos), x)
+    lab = oracle.to_natural(np.arange(S, dtype=np.float64)[:, None][pos], pos)
+    np.testing.assert_array_equal(lab[:, 0], np.arange(S))
+    if layout == CONTIGUOUS:
+        np.testing.assert_array_equal(oracle.to_natural(x, pos), x)
