@@ -201,11 +201,17 @@ def run_ours(args, wl):
         lse_parts = torch.empty((N,) + tuple(lse_l.shape), dtype=torch.float32, device=dev)
         comm = torch.cuda.Stream(device=dev)
         launches_per_step = 5 + N + 1   # permutes, one forward launch per ring step, the merge
+    if args.path == "allgather":
+        k_all, v_all = torch.empty_like(k), torch.empty_like(v)
+        launches_per_step = 5 + 2 + 1   # permutes, the K and V gathers, the forward
 
     def forward(qx, kx, vx):
         if args.path == "ring":
             ra.ra_ring_fwd(plan, qx, kx, vx, o=o_l, lse=lse_l, k_buf=kbuf, v_buf=vbuf, o_parts=o_parts,
                            lse_parts=lse_parts, comm_stream=comm)
+        elif args.path == "allgather":
+            ra.ra_allgather_kv(plan, kx, vx, k_all, v_all)
+            ra.ra_fwd_gathered(plan, qx, k_all, v_all, o=o_l, lse=lse_l)
         else:
             ra.ra_fwd(plan, qx, kx, vx, o=o_l, lse=lse_l)
 
@@ -377,6 +383,10 @@ def run_ours(args, wl):
         peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         backward["frac_of_sustained"] = backward["TFLOP/s"] / peak_s
         line["backward"] = backward
+    if args.path == "allgather":
+        line["config"]["path"] = "all-gather variant: K/V gathered into natural order, one step over all keys"
+        line["roofline"]["kernel"] = "fwd_bf16_kernel (gathered K/V) + 2 gathers"
+        line["roofline"]["traffic"] = None
     if ring is not None:
         line["ring_driver"] = ring
         line["config"]["path"] = "ring driver: per-step launches, K/V exchange on a second stream, merge"
@@ -552,9 +562,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip the permute/merge bandwidth lines")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
-    ap.add_argument("--path", default="fused", choices=["fused", "ring"],
+    ap.add_argument("--path", default="fused", choices=["fused", "ring", "allgather"],
                     help="fused: one ra_fwd launch per step; ring: the explicit ring driver "
-                         "(per-step launches, K/V exchange on a second stream, merge)")
+                         "(per-step launches, K/V exchange on a second stream, merge); allgather: "
+                         "K/V gathered into natural order, then one step over all keys")
     args = ap.parse_args()
     from context_ring_attention_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]

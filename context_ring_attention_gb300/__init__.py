@@ -22,6 +22,7 @@ __all__ = [
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
     "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
+    "ra_allgather_kv", "ra_fwd_gathered",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -31,7 +32,8 @@ _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_
            4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size")
+            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
+            "ra_allgather_kv", "ra_fwd_gathered")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -81,6 +83,8 @@ def load_library():
         "ra_ring_fwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
         "ra_bwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
         "ra_bwd_scratch_size": ([P, VP], I32),
+        "ra_allgather_kv": ([P, VP, VP, VP, VP, VP], I32),
+        "ra_fwd_gathered": ([P, VP, VP, VP, VP, VP, VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -376,3 +380,31 @@ def ra_bwd_scratch_size(plan):
     n = ctypes.c_int64()
     _check(load_library().ra_bwd_scratch_size(plan.handle, ctypes.byref(n)))
     return n.value
+
+
+def ra_allgather_kv(plan, k, v, k_all=None, v_all=None, stream=None):
+    """Gather every shard's K/V block into one natural-order copy -> (k_all, v_all)."""
+    import torch
+    _check_qkv(plan, k=k, v=v)
+    if k_all is None:
+        k_all = torch.empty_like(k)
+    if v_all is None:
+        v_all = torch.empty_like(v)
+    _check_qkv(plan, k_all=k_all, v_all=v_all)
+    _check(load_library().ra_allgather_kv(plan.handle, _ptr(k), _ptr(v), _ptr(k_all), _ptr(v_all),
+                                          _stream(stream)))
+    return k_all, v_all
+
+
+def ra_fwd_gathered(plan, q, k_all, v_all, o=None, lse=None, stream=None):
+    """Forward of the all-gather variant: layout-order q against natural-order K/V -> (O, LSE)."""
+    import torch
+    pb = plan.problem
+    _check_qkv(plan, q=q, k_all=k_all, v_all=v_all)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((pb["batch"], pb["heads_q"], pb["seq"]), dtype=torch.float32, device=q.device)
+    _check(load_library().ra_fwd_gathered(plan.handle, _ptr(q), _ptr(k_all), _ptr(v_all), _ptr(o), _ptr(lse),
+                                          _stream(stream)))
+    return o, lse

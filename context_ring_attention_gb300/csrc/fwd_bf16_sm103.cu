@@ -129,29 +129,45 @@ __device__ __forceinline__ void drain_bar(const Ctl& c, uint32_t bar, uint32_t p
   }
 }
 
+// Key tiles a query tile whose largest position is maxq visits in the key block it
+// meets: shard r of the ring, or (gathered) the one natural-order block of S keys.
+template <bool kGathered>
+__device__ __forceinline__ int kv_tiles(const FwdParams& P, int r, int64_t maxq) {
+  return kGathered ? visit_tiles(RA_LAYOUT_CONTIGUOUS, 1, P.seq, P.causal, 0, maxq)
+                   : visit_tiles(P.layout, P.n_shards, P.s_n, P.causal, r, maxq);
+}
+
 // Position in the virtual ring: step t, key shard r, key tile kt of nt.
 struct Walk {
   int t, r, kt, nt;
 };
 
+template <bool kGathered>
 __device__ __forceinline__ void walk_to_next_step(Walk& w, const FwdParams& P, int p, int64_t maxq) {
-  for (++w.t; w.t < P.step_hi; ++w.t) {
-    w.r = (p - w.t + P.n_shards) % P.n_shards;
-    w.nt = visit_tiles(P.layout, P.n_shards, P.s_n, P.causal, w.r, maxq);
+  for (++w.t; w.t < (kGathered ? P.step_lo + 1 : P.step_hi); ++w.t) {
+    if (kGathered) {  // one gathered block: shard 0 of S natural-order rows
+      w.r = 0;
+      w.nt = visit_tiles(RA_LAYOUT_CONTIGUOUS, 1, P.seq, P.causal, 0, maxq);
+    } else {
+      w.r = (p - w.t + P.n_shards) % P.n_shards;
+      w.nt = visit_tiles(P.layout, P.n_shards, P.s_n, P.causal, w.r, maxq);
+    }
     if (w.nt > 0) {
       w.kt = 0;
       return;
     }
   }
 }
+template <bool kGathered>
 __device__ __forceinline__ void walk_begin(Walk& w, const FwdParams& P, int p, int64_t maxq) {
   w.t = P.step_lo - 1;
   w.kt = 0;
   w.nt = 0;
-  walk_to_next_step(w, P, p, maxq);
+  walk_to_next_step<kGathered>(w, P, p, maxq);
 }
+template <bool kGathered>
 __device__ __forceinline__ void walk_advance(Walk& w, const FwdParams& P, int p, int64_t maxq) {
-  if (++w.kt >= w.nt) walk_to_next_step(w, P, p, maxq);
+  if (++w.kt >= w.nt) walk_to_next_step<kGathered>(w, P, p, maxq);
 }
 
 // ------------------------------------------------------------- work items --
@@ -210,6 +226,7 @@ __device__ __forceinline__ bool barrier_wait(const Ctl& c, const uint32_t* count
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+template <bool kGathered>
 __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
                              const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                              ProducerState& st) {
@@ -256,11 +273,11 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
     const int kvh = (it.bh0 % P.heads_q) / P.group;
     const int64_t kv_base = (int64_t)(b * P.heads_kv + kvh) * P.seq;
     Walk w;
-    walk_begin(w, P, it.shard, it.maxq);
+    walk_begin<kGathered>(w, P, it.shard, it.maxq);
     bool ok = true;
     while (ok && w.t < P.step_hi) {
       const int slot = P.kv_rotated ? it.shard : w.r;  // where the block of step t sits
-      const int32_t y = (int32_t)(kv_base + (int64_t)slot * P.s_n + (int64_t)w.kt * kTileRows);
+      const int32_t y = (int32_t)(kv_base + (kGathered ? 0 : (int64_t)slot * P.s_n) + (int64_t)w.kt * kTileRows);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // K tile, then V tile
         const uint32_t s = kv_it % kStages, use = kv_it / kStages;
@@ -275,7 +292,7 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
         TMA_KV(dst + kHalfBytes, map, c.bar(kKVFull + s), 64, y);
         st.kv_issued = ++kv_it;
       }
-      walk_advance(w, P, it.shard, it.maxq);
+      walk_advance<kGathered>(w, P, it.shard, it.maxq);
     }
     if (!ok) break;
     if (P.round_sync) {
@@ -314,6 +331,7 @@ __device__ __forceinline__ void issue_pv(const Descs& dl, uint32_t tmem, int g, 
   }
 }
 
+template <bool kGathered>
 __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots, uint32_t tmem) {
   const bool partials = P.o_parts != nullptr;
   Descs dl;
@@ -331,7 +349,7 @@ __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volati
     // already orders the async-proxy writes before the MMAs that read them.
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kQFull), u & 1u, kStatusTimeoutMma))) return;
     Walk cur;
-    walk_begin(cur, P, it.shard, it.maxq);
+    walk_begin<kGathered>(cur, P, it.shard, it.maxq);
     if (cur.t >= P.step_hi) {
       ptx::mma_commit_warp(c.bar(kQEmpty));
       continue;
@@ -349,7 +367,7 @@ __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volati
     bool first_tile = true;
     for (;;) {
       Walk nxt = cur;
-      walk_advance(nxt, P, it.shard, it.maxq);
+      walk_advance<kGathered>(nxt, P, it.shard, it.maxq);
       const bool has_next = nxt.t < P.step_hi;
       const bool seg_first = partials ? (cur.kt == 0) : first_tile;
       const bool seg_last = partials ? (!has_next || nxt.t != cur.t) : !has_next;
@@ -435,6 +453,7 @@ __device__ __forceinline__ void store_segment(const FwdParams& P, uint32_t tO, f
   }
 }
 
+template <bool kGathered>
 __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, volatile int32_t* slots,
                             uint32_t tmem, int g, int wq, int lane) {
   const int row = wq * 32 + lane;  // TMEM lane = query row of the tile
@@ -459,14 +478,15 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
     const int64_t my_pos = pos_of(P.layout, N, P.s_n, p, valid ? i : P.s_n - 1);
     const int64_t out_row = (int64_t)bh * P.seq + (int64_t)p * P.s_n + i;
     int last_t = -1;
-    for (int t = P.step_lo; t < P.step_hi; ++t)
-      if (visit_tiles(P.layout, N, P.s_n, P.causal, (p - t + N) % N, it.maxq) > 0) last_t = t;
+    const int t_end = kGathered ? P.step_lo + 1 : P.step_hi;  // gathered: one step
+    for (int t = P.step_lo; t < t_end; ++t)
+      if (kv_tiles<kGathered>(P, (p - t + N) % N, it.maxq) > 0) last_t = t;
 
     float m = -INFINITY, l = 0.f;
     bool open = false;
-    for (int t = P.step_lo; t < P.step_hi; ++t) {
-      const int r = (p - t + N) % N;
-      const int nt = visit_tiles(P.layout, N, P.s_n, P.causal, r, it.maxq);
+    for (int t = P.step_lo; t < t_end; ++t) {
+      const int r = kGathered ? 0 : (p - t + N) % N;
+      const int nt = kv_tiles<kGathered>(P, r, it.maxq);
       const int part = t - P.step_lo;  // index of this step's partial
       if (nt == 0) {
         if (partials && valid) {  // nothing of this block is causal for the tile
@@ -476,14 +496,16 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
         }
         continue;
       }
-      const int64_t J = P.causal ? last_le(P.layout, N, P.s_n, r, my_pos) : P.s_n - 1;
+      const int64_t kv_rows = kGathered ? P.seq : P.s_n;  // rows of the key block met
+      const int64_t J = !P.causal ? kv_rows - 1
+                                  : (kGathered ? my_pos : last_le(P.layout, N, P.s_n, r, my_pos));
       for (int kt = 0; kt < nt; ++kt) {
         const bool first = partials ? (kt == 0) : !open;
         const bool last = partials ? (kt == nt - 1) : (t == last_t && kt == nt - 1);
         open = true;
         const int64_t j0 = (int64_t)kt * kTileRows;
         int64_t lim = J - j0 + 1;
-        const int64_t cap = (P.s_n - j0 < kTileRows) ? P.s_n - j0 : kTileRows;
+        const int64_t cap = (kv_rows - j0 < kTileRows) ? kv_rows - j0 : kTileRows;
         lim = lim < 0 ? 0 : (lim > cap ? cap : lim);
         const int limit = (int)lim;
 
@@ -582,6 +604,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
   }
 }
 
+template <bool kGathered>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const FwdParams P) {
@@ -631,12 +654,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     ptx::regs_release<kRegsOther>();
     if (warp == 0) {
-      run_producer(P, c, sbase, slots, &tq, &tk, &tv, ps);  // whole warp; one elected lane issues
+      run_producer<kGathered>(P, c, sbase, slots, &tq, &tk, &tv, ps);  // whole warp; one elected lane issues
       __syncwarp();
     } else if (warp == 1) {
       // The whole warp runs the MMA loop with warp-uniform values; one elected
       // lane issues each tcgen05 instruction.
-      run_mma(P, c, sbase, slots, tmem);
+      run_mma<kGathered>(P, c, sbase, slots, tmem);
       // Every MMA this warp issued must retire before TMEM is freed.
       ptx::mma_commit_warp(c.bar(kDone));
       drain_bar(c, c.bar(kDone), 0);
@@ -644,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     ptx::regs_acquire<kRegsSoftmax>();
-    run_softmax(P, c, sbase, slots, tmem, (warp - 4) >> 2, warp & 3, lane);
+    run_softmax<kGathered>(P, c, sbase, slots, tmem, (warp - 4) >> 2, warp & 3, lane);
   }
 
   if (warp == 0 && lane == 0 && *c.abort) {  // (every lane of warp 0 holds the same counts)
@@ -697,21 +720,11 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-int fwd_bf16_smem_bytes() { return (int)kSmemBytes; }
-
-cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, const void* v,
-                            int grid, cudaStream_t stream, const char** why) {
-  CUtensorMap tq, tk, tv;
-  const int64_t rows_q = (int64_t)prm.batch * prm.heads_q * prm.seq;
-  const int64_t rows_kv = (int64_t)prm.batch * prm.heads_kv * prm.seq;
-  if (!encode_rows(&tq, q, rows_q) || !encode_rows(&tk, k, rows_kv) || !encode_rows(&tv, v, rows_kv)) {
-    *why = "cuTensorMapEncodeTiled failed or is unavailable";
-    return cudaErrorInvalidValue;
-  }
+template <bool kGathered>
+cudaError_t launch_kernel(const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          int grid, cudaStream_t stream, const char** why) {
   cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_bf16_kernel);
+  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_bf16_kernel<kGathered>);
   if (e != cudaSuccess) {
     *why = "cudaFuncGetAttributes failed";
     return e;
@@ -721,7 +734,7 @@ cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, 
     *why = "kernel was built with fewer launch registers than its warpgroup split needs";
     return cudaErrorInvalidConfiguration;
   }
-  e = cudaFuncSetAttribute(fwd_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  e = cudaFuncSetAttribute(fwd_bf16_kernel<kGathered>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) {
     *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
@@ -739,14 +752,31 @@ cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, 
     coop[0].val.cooperative = 1;
     cfg.attrs = coop;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fwd_bf16_kernel, tq, tk, tv, prm);
+    e = cudaLaunchKernelEx(&cfg, fwd_bf16_kernel<kGathered>, tq, tk, tv, prm);
     if (e == cudaSuccess) e = cudaGetLastError();
   } else {
-    fwd_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
+    fwd_bf16_kernel<kGathered><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, prm);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) *why = "tensor-core forward launch failed";
   return e;
+}
+
+}  // namespace
+
+int fwd_bf16_smem_bytes() { return (int)kSmemBytes; }
+
+cudaError_t launch_fwd_bf16(const FwdParams& prm, const void* q, const void* k, const void* v,
+                            int grid, cudaStream_t stream, const char** why) {
+  CUtensorMap tq, tk, tv;
+  const int64_t rows_q = (int64_t)prm.batch * prm.heads_q * prm.seq;
+  const int64_t rows_kv = (int64_t)prm.batch * prm.heads_kv * prm.seq;
+  if (!encode_rows(&tq, q, rows_q) || !encode_rows(&tk, k, rows_kv) || !encode_rows(&tv, v, rows_kv)) {
+    *why = "cuTensorMapEncodeTiled failed or is unavailable";
+    return cudaErrorInvalidValue;
+  }
+  return prm.gathered ? launch_kernel<true>(prm, tq, tk, tv, grid, stream, why)
+                      : launch_kernel<false>(prm, tq, tk, tv, grid, stream, why);
 }
 
 }  // namespace ra

@@ -56,9 +56,11 @@ __global__ void __launch_bounds__(kWarps * 32)
 
   for (int t = P.step_lo; t < P.step_hi; ++t) {
     const int r = (p - t + N) % N;
-    // Keys of shard r with position <= my_pos are rows 0..J (positions rise with the row).
-    const int64_t nkeys = P.causal ? last_le(P.layout, N, P.s_n, r, my_pos) + 1 : P.s_n;
-    const int slot = P.kv_rotated ? p : r;  // where the block of step t sits
+    // Keys of shard r with position <= my_pos are rows 0..J (positions rise with the row);
+    // gathered K/V is one natural-order block of S keys: rows 0..my_pos.
+    const int64_t kv_rows = P.gathered ? P.seq : P.s_n;
+    const int64_t nkeys = !P.causal ? kv_rows : (P.gathered ? my_pos + 1 : last_le(P.layout, N, P.s_n, r, my_pos) + 1);
+    const int slot = P.gathered ? 0 : (P.kv_rotated ? p : r);  // where the block of step t sits
     const float* kb = k + (kv_base + (int64_t)slot * P.s_n) * d;
     const float* vb = v + (kv_base + (int64_t)slot * P.s_n) * d;
     for (int64_t j0 = 0; j0 < nkeys; j0 += 32) {

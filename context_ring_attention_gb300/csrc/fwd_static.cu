@@ -187,6 +187,7 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   prm.step_hi = (int16_t)prob->n_shards;
   prm.kv_rotated = 0;
   prm.round_sync = ra::use_round_sync(prob->seq, prob->head_dim, max_cost) ? 1 : 0;
+  prm.gathered = 0;
   if (n_items == 0) return RA_OK;
   const int grid = (int)std::min<int64_t>(n_items, g_dev_sms[dev] > 0 ? g_dev_sms[dev] : 148);
   const char* why = "";

@@ -28,6 +28,8 @@ struct ra_plan_s {
   std::vector<ra::WorkItem> items;       // whole forward: all N steps per item
   std::vector<ra::WorkItem> step_items;  // per-step lists, concatenated
   std::vector<ra::WorkItem> bwd_items;   // backward: key tiles (dK, dV), then query tiles (dQ)
+  std::vector<ra::WorkItem> gather_items;  // forward over gathered (natural-order) K/V
+  bool gather_round_sync = false;
   int64_t n_bwd_kv = 0;                  // how many of bwd_items are key tiles
   bool bwd_round_sync[2] = {false, false};  // per backward pass (ra::use_round_sync)
   std::vector<int64_t> step_off;         // list of step t is [step_off[t], step_off[t+1])
@@ -36,6 +38,7 @@ struct ra_plan_s {
   ra::WorkItem* d_items = nullptr;
   ra::WorkItem* d_step_items = nullptr;
   ra::WorkItem* d_bwd_items = nullptr;
+  ra::WorkItem* d_gather_items = nullptr;
   uint32_t* d_status = nullptr;
   cudaEvent_t ev_entry = nullptr, ev_rot = nullptr, ev_step = nullptr;  // ra_ring_fwd ordering
   bool round_sync = false;  // forward kernel schedule (ra::use_round_sync)
@@ -282,6 +285,19 @@ void build_schedule(ra_plan_s* pl) {
 
   build_bwd_schedule(pl);
 
+  // The all-gather variant: the same items, each meeting one natural-order block of
+  // all S keys (the keys at or before its last query, when causal).
+  {
+    std::vector<Keyed> g = list;
+    int64_t gmax = 0;
+    for (Keyed& k : g) {
+      k.w.cost = ra::visit_tiles(RA_LAYOUT_CONTIGUOUS, 1, pb.seq, pb.causal, 0, k.w.maxq);
+      gmax = std::max<int64_t>(gmax, k.w.cost);
+    }
+    pl->gather_items = schedule(g, pb.heads_q, G);
+    pl->gather_round_sync = ra::use_round_sync(pb.seq, pb.head_dim, gmax);
+  }
+
   // One list per ring step: the same items, costed by that step's key tiles alone.
   // Items with no causal key in the step stay in the list (they write the empty
   // partial: O_t = 0, LSE_t = -inf).
@@ -332,6 +348,12 @@ ra_status upload(ra_plan_s* pl) {
       e = cudaMemcpy(pl->d_bwd_items, pl->bwd_items.data(), pl->bwd_items.size() * sizeof(ra::WorkItem),
                      cudaMemcpyHostToDevice);
   }
+  if (e == cudaSuccess && !pl->gather_items.empty()) {
+    e = cudaMalloc(&pl->d_gather_items, pl->gather_items.size() * sizeof(ra::WorkItem));
+    if (e == cudaSuccess)
+      e = cudaMemcpy(pl->d_gather_items, pl->gather_items.data(), pl->gather_items.size() * sizeof(ra::WorkItem),
+                     cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_entry, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_rot, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_step, cudaEventDisableTiming);
@@ -363,6 +385,7 @@ ra::FwdParams fwd_params(const ra_plan_s* plan) {
   prm.step_hi = (int16_t)pb.n_shards;
   prm.kv_rotated = 0;
   prm.round_sync = plan->round_sync ? 1 : 0;
+  prm.gathered = 0;
   return prm;
 }
 
@@ -466,6 +489,7 @@ ra_status ra_plan_destroy(ra_plan_t plan) {
     cudaFree(plan->d_items);
     cudaFree(plan->d_step_items);
     cudaFree(plan->d_bwd_items);
+    cudaFree(plan->d_gather_items);
     cudaFree(plan->d_status);
     if (plan->ev_entry) cudaEventDestroy(plan->ev_entry);
     if (plan->ev_rot) cudaEventDestroy(plan->ev_rot);
@@ -722,6 +746,51 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   }
   return ok();
+}
+
+ra_status ra_allgather_kv(ra_plan_t plan, const void* k, const void* v, void* k_all, void* v_all, void* stream) {
+  if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
+  const ra_problem& pb = plan->prob;
+  const void* ptrs[] = {k, v, k_all, v_all};
+  for (const void* p : ptrs) {
+    if (p == nullptr) return fail(RA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+  }
+  const size_t bytes = (size_t)pb.batch * pb.heads_kv * pb.seq * pb.head_dim * elem_bytes(pb);
+  if (overlap(k, k_all, bytes) || overlap(v, v_all, bytes) || overlap(k_all, v_all, bytes))
+    return fail(RA_ERR_INVALID_ARG, "a destination overlaps its source or the other destination");
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int row_bytes = pb.head_dim * (int)elem_bytes(pb);
+  const int64_t outer = pb.batch * (int64_t)pb.heads_kv;
+  // layout order -> natural order: every shard's rows land at their positions
+  cudaError_t e = ra::launch_layout_perm(pb.layout, pb.seq, pb.n_shards, 1, outer, row_bytes, k, k_all, st);
+  if (e == cudaSuccess) e = ra::launch_layout_perm(pb.layout, pb.seq, pb.n_shards, 1, outer, row_bytes, v, v_all, st);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "gather launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+ra_status ra_fwd_gathered(ra_plan_t plan, const void* q, const void* k_all, const void* v_all, void* o, float* lse,
+                          void* stream) {
+  if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
+  if (q == nullptr || k_all == nullptr || v_all == nullptr || o == nullptr)
+    return fail(RA_ERR_INVALID_ARG, "null pointer");
+  const void* ptrs[] = {q, k_all, v_all, o, lse};
+  for (const void* p : ptrs)
+    if (p != nullptr && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+  ra_status s = check_device(plan);
+  if (s != RA_OK) return s;
+  ra::FwdParams prm = fwd_params(plan);
+  prm.gathered = 1;
+  prm.step_lo = 0;
+  prm.step_hi = 1;
+  prm.items = plan->d_gather_items;
+  prm.n_items = (int32_t)plan->gather_items.size();
+  prm.round_sync = plan->gather_round_sync ? 1 : 0;
+  prm.o = o;
+  prm.lse = lse;
+  return launch(plan, prm, q, k_all, v_all, static_cast<cudaStream_t>(stream));
 }
 
 ra_status ra_sync_status(ra_plan_t plan, void* stream) {

@@ -113,11 +113,16 @@ struct FwdParams {
   // 0: the key/value block of step t for query shard p is read in place, at the rows
   // of shard r = (p - t) mod N.  1: it is read from shard p's own rows of a receive
   // buffer that holds, in slot p, the block shard p has been passed by step t.
-  int16_t kv_rotated;
+  int8_t kv_rotated;
   // 0: CTAs take work items from a counter as they free up.  1: round u gives CTA b
   // item u*grid + b and starts only when every CTA has issued the previous round's
   // loads (cooperative launch), so the CTAs of a round stream the same K/V in step.
-  int16_t round_sync;
+  int8_t round_sync;
+  // 1: K and V are one gathered block of all S keys in natural order (the
+  // all-gather variant): the key side is one contiguous shard of S rows, met in a
+  // single step.  0: K/V in the queries' layout, met shard by shard around the ring.
+  int8_t gathered;
+  int8_t pad_;
   const WorkItem* items;
   void* o;           // fused output, plan dtype
   float* lse;        // fused LSE or nullptr

@@ -245,6 +245,36 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
 ra_status ra_bwd_scratch_size(ra_plan_t plan, int64_t* bytes);
 
 /*
+ * ra_allgather_kv -- the all-gather of the all-gather variant of context parallelism:
+ * every device gathers the K/V blocks of all shards instead of passing them around
+ * a ring ("3.6 Distributed Training II", section "Ring Attention": the Llama 3
+ * paper's context parallelism for long-context training, with an all-gather of K/V
+ * rather than a ring).  One GPU keeps one gathered copy: k_all, v_all
+ * [B, Hkv, S, d] receive K and V in NATURAL order (row = token position).
+ * k, v: [B, Hkv, S, d] in layout order.  Device pointers, plan dtype, 16-byte
+ * aligned; a destination must not overlap its source or the other destination.
+ * Asynchronous on stream; allocates nothing.
+ * Errors: RA_ERR_INVALID_ARG (null/misaligned pointers, overlap), RA_ERR_NO_DEVICE,
+ * RA_ERR_CUDA.
+ */
+ra_status ra_allgather_kv(ra_plan_t plan, const void* k, const void* v, void* k_all, void* v_all,
+                          void* stream);
+
+/*
+ * ra_fwd_gathered -- the forward of the all-gather variant: every query row of
+ * shard p attends over the gathered K/V in one step, causal by position (the keys
+ * at or before its own position; Module 23, "Exact by Construction").  The result
+ * is the same attention as ra_fwd; only the data movement differs.
+ * q: [B, Hq, S, d] in layout order; k_all, v_all: [B, Hkv, S, d] in natural order
+ * (ra_allgather_kv); o [B, Hq, S, d] (plan dtype) and lse [B, Hq, S] float32 (may be
+ * NULL) in layout order.  Device pointers, 16-byte aligned.  Asynchronous on stream;
+ * allocates nothing.  Calls that share a plan must not overlap on the GPU.
+ * Errors: RA_ERR_INVALID_ARG (null/misaligned pointers), RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ */
+ra_status ra_fwd_gathered(ra_plan_t plan, const void* q, const void* k_all, const void* v_all,
+                          void* o, float* lse, void* stream);
+
+/*
  * ra_merge_partials -- exact combination of partial attention results.
  * For each of `rows` rows: LSE = ln sum_t e^(LSE_t), O = sum_t e^(LSE_t - LSE) O_t
  * (order independence of the online-softmax fold, Module 23, "The Math: One
