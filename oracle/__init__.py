@@ -43,6 +43,9 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
                             cases, causal and not, with grouped heads; a single key gives
                             dV = dO and dQ = dK = 0; the rows of dK sum to zero.
 ``ring_backward``           equals ``attention_backward`` for every layout, causal and not.
+``ulysses_seq_to_head``,    labelled rows land on the device of their head at their position;
+``ulysses_head_to_seq``     the two exchanges are inverse; exchange, per-device attention,
+                            exchange back equals attention over the whole sequence.
 ``merge_partials``          splitting the keys into halves and merging reproduces
                             ``full_attention``; -inf parts are ignored.
 ``tile_counts``             brute force over every (q, k) pair of every tile on small
@@ -57,6 +60,7 @@ from .attention import attention_rows, full_attention, full_attention_rows
 from .ring import ring_sim, ring_partials, pass_blocks, held_blocks
 from .merge import merge_partials
 from .backward import attention_backward, ring_backward
+from .ulysses import ulysses_seq_to_head, ulysses_head_to_seq
 from .tiles import tile_counts, tile_classes_bruteforce
 
 __all__ = [
@@ -64,6 +68,6 @@ __all__ = [
     "layout_positions", "causal_pair_counts", "to_natural",
     "full_attention", "full_attention_rows", "attention_rows",
     "ring_sim", "ring_partials", "pass_blocks", "held_blocks", "merge_partials",
-    "attention_backward", "ring_backward",
+    "attention_backward", "ring_backward", "ulysses_seq_to_head", "ulysses_head_to_seq",
     "tile_counts", "tile_classes_bruteforce",
 ]
