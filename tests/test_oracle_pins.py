@@ -453,20 +453,19 @@ def test_to_natural_inverts_the_layout(layout):
 @pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
 def test_ulysses_exchange(layout):
     N, B, H, S = 4, 2, 8, 32
-    s_n, hl = S // N, H // N
+    hl = H // N
     pos = layout_positions(layout, S, N)
-    # label = (b, h, position): after the exchange device h // hl holds head h at row = position
-    x = np.zeros((N, B, H, s_n, 3))
-    for p in range(N):
-        for i in range(s_n):
-            x[p, :, :, i, 0] = np.arange(B)[:, None]
-            x[p, :, :, i, 1] = np.arange(H)[None, :]
-            x[p, :, :, i, 2] = pos[p * s_n + i]
+    # label = (b, h, position) on the layout-ordered sequence side
+    x = np.zeros((B, H, S, 3))
+    x[..., 0] = np.arange(B)[:, None, None]
+    x[..., 1] = np.arange(H)[None, :, None]
+    x[..., 2] = pos[None, None, :]
     y = oracle.ulysses_seq_to_head(x, pos, N)
-    for q in range(N):
+    for q in range(N):            # device q holds heads q*hl.., every position in order
         for hh in range(hl):
             np.testing.assert_array_equal(y[q, :, hh, :, 1], q * hl + hh)
             np.testing.assert_array_equal(y[q, :, hh, :, 2], np.broadcast_to(np.arange(S), (B, S)))
+            np.testing.assert_array_equal(y[q, :, hh, :, 0], np.broadcast_to(np.arange(B)[:, None], (B, S)))
     np.testing.assert_array_equal(oracle.ulysses_head_to_seq(y, pos, N), x)
 
 
@@ -476,12 +475,10 @@ def test_ulysses_attention_equals_full():
     pos = layout_positions(ZIGZAG, S, N)
     q, k, v = _rand((B, Hq, S, d), 110), _rand((B, Hkv, S, d), 111), _rand((B, Hkv, S, d), 112)
     ql, kl, vl = q[..., pos, :], k[..., pos, :], v[..., pos, :]        # layout order
-    s_n = S // N
-    shard = lambda t: np.stack([t[:, :, p * s_n:(p + 1) * s_n] for p in range(N)])  # [N, B, H, S/N, d]
-    qh, kh, vh = (oracle.ulysses_seq_to_head(shard(t), pos, N) for t in (ql, kl, vl))
+    qh, kh, vh = (oracle.ulysses_seq_to_head(t, pos, N) for t in (ql, kl, vl))
     outs, lses = zip(*(full_attention(qh[p], kh[p], vh[p], causal=True) for p in range(N)))
     o = oracle.ulysses_head_to_seq(np.stack(outs), pos, N)
     lse = oracle.ulysses_head_to_seq(np.stack(lses)[..., None], pos, N)[..., 0]
     ow, lw = full_attention(ql, kl, vl, causal=True, positions=pos)
-    np.testing.assert_allclose(np.concatenate(list(o), axis=2), ow, atol=1e-12)
-    np.testing.assert_allclose(np.concatenate(list(lse), axis=2), lw, atol=1e-12)
+    np.testing.assert_allclose(o, ow, atol=1e-12)
+    np.testing.assert_allclose(lse, lw, atol=1e-12)
