@@ -204,6 +204,14 @@ def run_ours(args, wl):
     if args.path == "allgather":
         k_all, v_all = torch.empty_like(k), torch.empty_like(v)
         launches_per_step = 5 + 2 + 1   # permutes, the K and V gathers, the forward
+    if args.path == "ulysses":
+        Hl, Hkl = wl.heads_q // N, wl.heads_kv // N
+        uplan = ra.ra_plan(N * wl.batch, wl.seq, Hl, Hkl, wl.head_dim, 1, "contiguous", wl.causal, wl.dtype)
+        qh = torch.empty((N, wl.batch, Hl, wl.seq, wl.head_dim), dtype=q.dtype, device=dev)
+        kh = torch.empty((N, wl.batch, Hkl, wl.seq, wl.head_dim), dtype=q.dtype, device=dev)
+        vh, oh = torch.empty_like(kh), torch.empty_like(qh)
+        lh = torch.empty((N, wl.batch, Hl, wl.seq), dtype=torch.float32, device=dev)
+        launches_per_step = 5 + 3 + 1 + 2   # permutes, 3 exchanges, the forward, 2 exchanges back
 
     def forward(qx, kx, vx):
         if args.path == "ring":
@@ -212,6 +220,14 @@ def run_ours(args, wl):
         elif args.path == "allgather":
             ra.ra_allgather_kv(plan, kx, vx, k_all, v_all)
             ra.ra_fwd_gathered(plan, qx, k_all, v_all, o=o_l, lse=lse_l)
+        elif args.path == "ulysses":
+            for src, dst in ((qx, qh), (kx, kh), (vx, vh)):
+                ra.ra_ulysses_a2a(src, layout, N, 0, out=dst)
+            B_ = N * wl.batch
+            ra.ra_fwd(uplan, qh.view(B_, Hl, wl.seq, -1), kh.view(B_, Hkl, wl.seq, -1), vh.view(B_, Hkl, wl.seq, -1),
+                      o=oh.view(B_, Hl, wl.seq, -1), lse=lh.view(B_, Hl, wl.seq))
+            ra.ra_ulysses_a2a(oh, layout, N, 1, out=o_l)
+            ra.ra_ulysses_a2a(lh, layout, N, 1, out=lse_l)
         else:
             ra.ra_fwd(plan, qx, kx, vx, o=o_l, lse=lse_l)
 
@@ -346,6 +362,10 @@ def run_ours(args, wl):
     if not args.no_bwd:
         backward = backward_report(ra, torch, plan, (ql, kl, vl), (o_l, lse_l), stream, flops, pg)
 
+    ulysses = None
+    if args.path == "ulysses":
+        ulysses = ulysses_report(ra, torch, layout, N, (ql, kl, vl), (o_l, lse_l), (qh, kh, vh, oh, lh), stream)
+
     ring = None
     if args.path == "ring":
         ring = ring_driver_report(ra, torch, plan, N, (ql, kl, vl), (o_l, lse_l), (kbuf, vbuf),
@@ -383,6 +403,15 @@ def run_ours(args, wl):
         peak_s = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         backward["frac_of_sustained"] = backward["TFLOP/s"] / peak_s
         line["backward"] = backward
+    if ulysses is not None:
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        ulysses["in_frac_of_hbm"] = ulysses["exchange_in_GB/s"] / hbm
+        ulysses["out_frac_of_hbm"] = ulysses["exchange_out_GB/s"] / hbm
+        line["ulysses"] = ulysses
+    if args.path == "ulysses":
+        line["config"]["path"] = "ulysses: all-to-all to head shards, one-shard attention per device, all-to-all back"
+        line["roofline"]["kernel"] = "fwd_bf16_kernel (one shard, batch N*B, H/N heads) + 5 exchanges"
+        line["roofline"]["traffic"] = None
     if args.path == "allgather":
         line["config"]["path"] = "all-gather variant: K/V gathered into natural order, one step over all keys"
         line["roofline"]["kernel"] = "fwd_bf16_kernel (gathered K/V) + 2 gathers"
@@ -478,6 +507,37 @@ def backward_report(ra, torch, plan, qkv, out, stream, flops, pg):
             "launches": 3}
 
 
+def ulysses_report(ra, torch, layout, N, seq_side, out_side, head_side, stream, reps=3):
+    """Bandwidth of Ulysses' exchanges: Q, K, V to head shards, then O and the LSE back."""
+    ql, kl, vl = seq_side
+    o_l, lse_l = out_side
+    qh, kh, vh, oh, lh = head_side
+
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def ex_in():
+        for src, dst in ((ql, qh), (kl, kh), (vl, vh)):
+            ra.ra_ulysses_a2a(src, layout, N, 0, out=dst)
+
+    def ex_out():
+        ra.ra_ulysses_a2a(oh, layout, N, 1, out=o_l)
+        ra.ra_ulysses_a2a(lh, layout, N, 1, out=lse_l)
+
+    t_in, t_out = timed(ex_in), timed(ex_out)
+    b_in = 2 * sum(t.numel() * t.element_size() for t in (ql, kl, vl))
+    b_out = 2 * (o_l.numel() * o_l.element_size() + lse_l.numel() * lse_l.element_size())
+    return {"exchange_in_ms": t_in, "exchange_in_GB/s": b_in / t_in / 1e6,
+            "exchange_out_ms": t_out, "exchange_out_GB/s": b_out / t_out / 1e6}
+
+
 def ring_driver_report(ra, torch, plan, N, qkv, out, bufs, parts, stream, driver_ms, flops):
     """Where the explicit ring driver's time goes: its pieces timed one by one.
 
@@ -562,10 +622,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernels", action="store_true", help="skip the permute/merge bandwidth lines")
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward-pass measurement")
-    ap.add_argument("--path", default="fused", choices=["fused", "ring", "allgather"],
+    ap.add_argument("--path", default="fused", choices=["fused", "ring", "allgather", "ulysses"],
                     help="fused: one ra_fwd launch per step; ring: the explicit ring driver "
                          "(per-step launches, K/V exchange on a second stream, merge); allgather: "
-                         "K/V gathered into natural order, then one step over all keys")
+                         "K/V gathered into natural order, then one step over all keys; ulysses: all-to-all to head "
+                         "shards, one-shard attention per device, all-to-all back")
     args = ap.parse_args()
     from context_ring_attention_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]

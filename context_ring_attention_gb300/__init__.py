@@ -22,7 +22,7 @@ __all__ = [
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
     "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
-    "ra_allgather_kv", "ra_fwd_gathered",
+    "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -33,7 +33,7 @@ _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
             "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
-            "ra_allgather_kv", "ra_fwd_gathered")
+            "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -85,6 +85,7 @@ def load_library():
         "ra_bwd_scratch_size": ([P, VP], I32),
         "ra_allgather_kv": ([P, VP, VP, VP, VP, VP], I32),
         "ra_fwd_gathered": ([P, VP, VP, VP, VP, VP, VP], I32),
+        "ra_ulysses_a2a": ([I32, I32, I64, I32, I64, I32, I32, VP, VP, VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -408,3 +409,25 @@ def ra_fwd_gathered(plan, q, k_all, v_all, o=None, lse=None, stream=None):
     _check(load_library().ra_fwd_gathered(plan.handle, _ptr(q), _ptr(k_all), _ptr(v_all), _ptr(o), _ptr(lse),
                                           _stream(stream)))
     return o, lse
+
+
+def ra_ulysses_a2a(x, layout, n_shards, direction, out=None, stream=None):
+    """Ulysses' exchange.  direction 0: [B, H, S, ...] layout order -> [N, B, H/N, S, ...];
+    direction 1: back.  Rows are d = 128 bf16 ([..., 128]) or one float32 ([...])."""
+    import torch
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    N = int(n_shards)
+    if direction == 0:
+        B, H, S = x.shape[:3]
+        out_shape = (N, B, H // N, S) + tuple(x.shape[3:])
+    else:
+        n_, B, hl, S = x.shape[:4]
+        H = hl * N
+        out_shape = (B, H, S) + tuple(x.shape[4:])
+    row_bytes = int(np.prod(x.shape[3 if direction == 0 else 4:], dtype=np.int64)) * x.element_size()
+    if out is None:
+        out = torch.empty(out_shape, dtype=x.dtype, device=x.device)
+    _check(load_library().ra_ulysses_a2a(int(direction), _layout(layout), int(S), N, int(B), int(H), row_bytes,
+                                         _ptr(x), _ptr(out), _stream(stream)))
+    return out

@@ -793,6 +793,27 @@ ra_status ra_fwd_gathered(ra_plan_t plan, const void* q, const void* k_all, cons
   return launch(plan, prm, q, k_all, v_all, static_cast<cudaStream_t>(stream));
 }
 
+ra_status ra_ulysses_a2a(int32_t direction, int32_t layout, int64_t seq, int32_t n_shards, int64_t batch,
+                          int32_t heads, int32_t row_bytes, const void* src, void* dst, void* stream) {
+  ra_status s = check_layout(layout, seq, n_shards);
+  if (s != RA_OK) return s;
+  if (direction != 0 && direction != 1) return fail(RA_ERR_INVALID_ARG, "direction must be 0 or 1");
+  if (batch < 1 || heads < 1 || heads % n_shards)
+    return fail(RA_ERR_INVALID_ARG, "batch >= 1 and heads a positive multiple of n_shards required");
+  if (row_bytes != 256 && row_bytes != 4)
+    return fail(RA_ERR_UNSUPPORTED, "row_bytes must be 256 (d = 128 bf16) or 4 (one float)");
+  if (batch * (int64_t)heads * seq > INT32_MAX || batch > INT32_MAX)
+    return fail(RA_ERR_UNSUPPORTED, "B*H*S above 2^31-1 rows");
+  if (src == nullptr || dst == nullptr) return fail(RA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_INVALID_ARG, "src/dst must be 16-byte aligned");
+  if (overlap(src, dst, (size_t)(batch * heads * seq) * row_bytes))
+    return fail(RA_ERR_INVALID_ARG, "src and dst overlap");
+  cudaError_t e = ra::launch_ulysses_a2a(direction, layout, n_shards, (int)batch, heads, seq, row_bytes, src, dst,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "exchange launch failed: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 ra_status ra_sync_status(ra_plan_t plan, void* stream) {
   if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
   if (plan->device < 0) return fail(RA_ERR_NO_DEVICE, "plan was built without a CUDA device");

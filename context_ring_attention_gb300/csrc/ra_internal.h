@@ -204,6 +204,9 @@ cudaError_t launch_bwd_f32(const BwdParams& prm, const float* q, const float* k,
 cudaError_t launch_bwd_bf16(int pass, const BwdParams& prm, const void* q, const void* k, const void* v,
                             const void* dout, int grid, cudaStream_t stream, const char** why);
 
+cudaError_t launch_ulysses_a2a(int dir, int layout, int n, int batch, int heads, int64_t seq, int row_bytes,
+                               const void* src, void* dst, cudaStream_t stream);
+
 // Sets the thread-local message returned by ra_last_error().
 void set_last_error(const char* msg);
 

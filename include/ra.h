@@ -275,6 +275,26 @@ ra_status ra_fwd_gathered(ra_plan_t plan, const void* q, const void* k_all, cons
                           void* o, float* lse, void* stream);
 
 /*
+ * ra_ulysses_a2a -- DeepSpeed-Ulysses' all-to-all for N devices (the Q&A page
+ * "Explain ring attention ...", section "Related approaches": split by attention
+ * heads with an all-to-all instead of a ring).  Each device starts with its
+ * sequence shard of every head; the exchange hands device p' every token, by
+ * position, of heads p'*H/N .. (p'+1)*H/N - 1, where it runs ordinary attention over
+ * the whole sequence (ra_fwd with a plan of batch N*B, H/N heads, one shard); the
+ * reverse exchange returns O (and the LSE) to the sequence shards.
+ * direction 0 (sequence -> heads): src [B, H, S, row] in layout order (shard p =
+ *   rows [p*S/N, (p+1)*S/N)), dst [N, B, H/N, S, row] (device p', natural order).
+ * direction 1 (heads -> sequence): src [N, B, H/N, S, row], dst [B, H, S, row].
+ * row_bytes: 256 (d = 128 bf16) or 4 (the float32 LSE).  heads: H, a multiple of N.
+ * Device pointers, 16-byte aligned, not overlapping.  Asynchronous; allocates nothing.
+ * Errors: RA_ERR_INVALID_ARG (uneven shards, heads % N, direction, pointers),
+ * RA_ERR_UNSUPPORTED (row_bytes, more than 2^31-1 rows), RA_ERR_CUDA.
+ */
+ra_status ra_ulysses_a2a(int32_t direction, int32_t layout, int64_t seq, int32_t n_shards,
+                         int64_t batch, int32_t heads, int32_t row_bytes, const void* src, void* dst,
+                         void* stream);
+
+/*
  * ra_merge_partials -- exact combination of partial attention results.
  * For each of `rows` rows: LSE = ln sum_t e^(LSE_t), O = sum_t e^(LSE_t - LSE) O_t
  * (order independence of the online-softmax fold, Module 23, "The Math: One

@@ -29,7 +29,7 @@ def _declared_symbols():
     with open(os.path.join(ROOT, "include", "ra.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ra_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ra_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
