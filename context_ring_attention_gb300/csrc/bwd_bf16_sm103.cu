@@ -67,13 +67,13 @@ constexpr uint32_t kLseBytes = 128 * 4;          // 64 lse2 values, then 64 D va
 
 template <int kPass>
 struct Cfg {
-  static constexpr int kStages = kPass == 0 ? 4 : 5;
-  static constexpr int kBufs = kPass == 0 ? 2 : 3;  // score/dP buffers in tensor memory
+  static constexpr int kStages = kPass == 0 ? 4 : 6;
+  static constexpr int kBufs = 2;  // score/dP buffers in tensor memory
   static constexpr uint32_t kStageBytes = kPass == 0 ? 2 * kStrBytes + 1024 : 2 * kStrBytes;
-  static constexpr uint32_t kOffFix = 0;
-  static constexpr uint32_t kOffStage = 2 * kFixBytes;
+  static constexpr uint32_t kOffFix = 0;  // pass 0 only: K, V (pass 1 keeps Q, dO in tensor memory)
+  static constexpr uint32_t kOffStage = kPass == 0 ? 2 * kFixBytes : 0;
   static constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
-  static constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;
+  static constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // barriers + slots, 1 KiB alignment slack
 };
 
 enum : int {
@@ -97,10 +97,11 @@ constexpr int kItemSlots = 4;
 constexpr uint32_t kItemConsumers = 9;  // MMA warp + 8 elementwise warps
 
 constexpr uint32_t kTmemCols = 512;
-// pass 0: dV at 256, dK at 384; pass 1: dQ at 384
+// pass 0: dV at 256, dK at 384; pass 1: dQ at 256, the item's Q at 384 and dO at 448
 template <int kPass>
-__device__ __forceinline__ uint32_t col_acc0() { return kPass == 0 ? 256u : 384u; }
+__device__ __forceinline__ uint32_t col_acc0() { return 256u; }
 constexpr uint32_t kColAcc1 = 384;
+constexpr uint32_t kColQ = 384, kColDO = 448;
 __device__ __forceinline__ uint32_t col_buf(uint32_t b) { return b * 128u; }
 constexpr uint32_t kColDP = 64;   // dP within a buffer; dS is written over its first 32 columns
 constexpr uint32_t kIdescSS = ptx::idesc_bf16_f32(128, 64, false, false);
@@ -294,15 +295,18 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
     if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
     if (idx < 0) break;
     const WorkItem it = P.items[idx];
-    if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
-    // The item's own tiles: rows bh0*S + shard*s_n + row0 of K and V (pass 0) or Q and dO (pass 1).
-    const int32_t yf = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
-    ptx::mbar_arrive_expect_tx_warp(c.bar(kFixFull), 2 * kFixBytes);
-    ptx::tma_load_2d_warp(sbase + C::kOffFix, tx0, c.bar(kFixFull), 0, yf);
-    ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixHalf, tx0, c.bar(kFixFull), 64, yf);
-    ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixBytes, tx1, c.bar(kFixFull), 0, yf);
-    ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixBytes + kFixHalf, tx1, c.bar(kFixFull), 64, yf);
-    st.fix_issued = u + 1;
+    if (kPass == 0) {
+      if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
+      // The item's own tiles: rows bh0*S + shard*s_n + row0 of K and V.  (Pass 1's own
+      // Q and dO rows go to tensor memory through the elementwise warps.)
+      const int32_t yf = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
+      ptx::mbar_arrive_expect_tx_warp(c.bar(kFixFull), 2 * kFixBytes);
+      ptx::tma_load_2d_warp(sbase + C::kOffFix, tx0, c.bar(kFixFull), 0, yf);
+      ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixHalf, tx0, c.bar(kFixFull), 64, yf);
+      ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixBytes, tx1, c.bar(kFixFull), 0, yf);
+      ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixBytes + kFixHalf, tx1, c.bar(kFixFull), 64, yf);
+      st.fix_issued = u + 1;
+    }
     // Streamed tiles.
     int b, h_base;
     if (kPass == 0) {  // bh0 = b * Hkv + kv head; queries of heads kv*G .. kv*G + G-1
@@ -349,7 +353,10 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
 // --------------------------------------------------------------------- MMA --
 template <int kPass>
 __device__ __forceinline__ void issue_ss(uint32_t tmem, int buf, uint32_t fix_lo, uint32_t str_lo) {
-  // Scores: fixed tile 0 x streamed tile 0; dP: fixed tile 1 x streamed tile 1.
+  // Scores: own tile 0 x streamed tile 0; dP: own tile 1 x streamed tile 1.  Pass 0's
+  // own tiles (K, V) are in shared memory; pass 1's (Q, dO) in tensor memory, two bf16
+  // of d per column, so its products read only the streamed 64-row tile from shared
+  // memory.
 #pragma unroll
   for (int which = 0; which < 2; ++which) {
     const uint32_t a0 = fix_lo + (which ? (kFixBytes >> 4) : 0u);
@@ -357,9 +364,13 @@ __device__ __forceinline__ void issue_ss(uint32_t tmem, int buf, uint32_t fix_lo
     const uint32_t d = tmem + col_buf(buf) + (which ? kColDP : 0u);
 #pragma unroll
     for (uint32_t kk = 0; kk < 8; ++kk) {  // 8 steps of K = 16 over d = 128
-      const uint32_t oa = ((kk >> 2) * kFixHalf + (kk & 3u) * 32u) >> 4;
       const uint32_t ob = ((kk >> 2) * kStrHalf + (kk & 3u) * 32u) >> 4;
-      ptx::mma_bf16_ss_lo_warp(d, a0 + oa, b0 + ob, kIdescSS, kk > 0 ? 1u : 0u);
+      if (kPass == 0) {
+        const uint32_t oa = ((kk >> 2) * kFixHalf + (kk & 3u) * 32u) >> 4;
+        ptx::mma_bf16_ss_lo_warp(d, a0 + oa, b0 + ob, kIdescSS, kk > 0 ? 1u : 0u);
+      } else {
+        ptx::mma_bf16_ts_lo_warp(d, tmem + (which ? kColDO : kColQ) + kk * 8u, b0 + ob, kIdescSS, kk > 0 ? 1u : 0u);
+      }
     }
   }
 }
@@ -399,6 +410,7 @@ __device__ void run_mma(const BwdParams& P, const Ctl& c, uint32_t sbase, volati
     const WorkItem it = P.items[idx];
     const uint32_t n = (uint32_t)item_tiles<kPass>(P, it);
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixFull), u & 1u, kStatusTimeoutMma))) return;
+    ptx::tc_fence_after();  // pass 1: Q and dO were stored into tensor memory by other warps
     // Run NB - 1 tiles ahead: buffer (J + NB - 1) % NB was last used by tile J - 1,
     // whose TS products are issued (the tensor pipe executes in issue order).
     for (uint32_t a = 0; a + 1 < NB && a < n; ++a)
@@ -489,10 +501,29 @@ __device__ void run_elementwise(const BwdParams& P, const Ctl& c, const uint8_t*
     const int64_t my_pos = pos_of(P.layout, N, P.s_n, it.shard, valid ? i_own : P.s_n - 1);
     const int64_t out_row = (int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + i_own;
     float2 own_l = make_float2(0.f, 0.f), own_d = make_float2(0.f, 0.f);  // pass 1: this row's lse2, D
-    if (kPass == 1 && valid) {
-      const int64_t li = bwd_scalar_index(it.bh0, it.shard, i_own, N, P.n64);
-      own_l = make_float2(P.lse2d[li], P.lse2d[li]);
-      own_d = make_float2(P.lse2d[li + 64], P.lse2d[li + 64]);
+    if (kPass == 1) {
+      if (valid) {
+        const int64_t li = bwd_scalar_index(it.bh0, it.shard, i_own, N, P.n64);
+        own_l = make_float2(P.lse2d[li], P.lse2d[li]);
+        own_d = make_float2(P.lse2d[li + 64], P.lse2d[li + 64]);
+      }
+      // This row of Q (warps 4-7) or dO (warps 8-11) into tensor memory, once the
+      // previous item's products are done with it.
+      const bool okq = wait_bar(c, c.bar(kFixEmpty), (u & 1u) ^ 1u, kStatusTimeoutSoftmax);
+      if (!__all_sync(0xffffffffu, okq)) return;
+      uint32_t words[64];
+      const uint4* src = reinterpret_cast<const uint4*>(g ? P.dout : P.q) + (valid ? out_row * 16 : 0);
+#pragma unroll
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const uint4 v4 = valid ? src[q4] : make_uint4(0u, 0u, 0u, 0u);
+        words[4 * q4] = v4.x;
+        words[4 * q4 + 1] = v4.y;
+        words[4 * q4 + 2] = v4.z;
+        words[4 * q4 + 3] = v4.w;
+      }
+      ptx::tmem_st64(tmem + lane_off + (g ? kColDO : kColQ), words);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(c.bar(kFixFull));
     }
 
     Walk w;
@@ -586,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const BwdParams P) {
   using C = Cfg<kPass>;
   using B = Bars<kPass>;
-  static_assert(8 * B::kNum + 8 + 4 * kItemSlots <= 256, "barrier area");
+  static_assert(8 * B::kNum + 8 + 4 * kItemSlots <= 512, "barrier area");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -597,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int32_t* slots = reinterpret_cast<volatile int32_t*>(sgen + off_slot + 8);
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(c.bar(kFixFull), 1);
+    ptx::mbar_init(c.bar(kFixFull), kPass == 0 ? 1 : 256);  // TMA (pass 0) or the 256 writers (pass 1)
     ptx::mbar_init(c.bar(kFixEmpty), 1);
     ptx::mbar_init(c.bar(kAccFull), 1);
     ptx::mbar_init(c.bar(kAccEmpty), 256);

@@ -718,6 +718,8 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;
+  prm.q = q;
+  prm.dout = dout;
   prm.status = plan->d_status;
   prm.item_counter = plan->d_status + 1;
   if (pb.dtype != RA_DTYPE_BF16) {

@@ -163,6 +163,8 @@ struct BwdParams {
   void* dq;             // [B, Hq, S, d], plan dtype
   void* dk;             // [B, Hkv, S, d]
   void* dv;
+  const void* q;        // pass 1 reads its own query rows of Q and dO directly
+  const void* dout;
   const WorkItem* items;
   uint32_t* status;
   uint32_t* item_counter;
