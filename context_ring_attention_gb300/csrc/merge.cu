@@ -1,7 +1,9 @@
 // Exact merge of partial attention results (order independence of the
 // online-softmax fold, Module 23, "The Math: One Block at a Time"):
 //   LSE = ln sum_t e^(LSE_t),   O = sum_t e^(LSE_t - LSE) O_t.
-// HBM-bound: one warp per row, 16-byte loads along d.
+// HBM-bound: one warp per row, 16-byte loads along d.  For d = 128 (the attention
+// case) a lane owns 4 columns; the part weights are computed once per row by the
+// lanes t < n_parts and broadcast, and eight parts' loads are in flight at once.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -77,6 +79,52 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// d = 128: lane owns columns 4*lane .. 4*lane + 3 of every part.
+template <bool kBf16Out>
+__global__ void __launch_bounds__(kWarps * 32)
+    merge_d128_kernel(int n_parts, int64_t rows, const float4* __restrict__ o_parts,
+                      const float* __restrict__ lse_parts, void* __restrict__ o, float* __restrict__ lse) {
+  constexpr int kBatch = 8;  // parts whose loads are in flight together
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  for (int64_t row = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); row < rows; row += stride) {
+    // lane t < n_parts (t < 32 here; more parts go through the generic kernel) holds LSE_t
+    const float lt = lane < n_parts ? lse_parts[(int64_t)lane * rows + row] : -INFINITY;
+    const float top = warp_max(lt);
+    const float e = (top != -INFINITY && lt != -INFINITY) ? expf(lt - top) : 0.f;
+    const float z = warp_sum(e);
+    const float big = (top != -INFINITY) ? top + logf(z) : -INFINITY;
+    const float w_lane = (big != -INFINITY && lt != -INFINITY) ? expf(lt - big) : 0.f;  // this lane's part weight
+    if (lane == 0 && lse != nullptr) lse[row] = big;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t0 = 0; t0 < n_parts; t0 += kBatch) {
+      float4 x[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b)
+        if (t0 + b < n_parts) x[b] = o_parts[((int64_t)(t0 + b) * rows + row) * 32 + lane];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const float w = __shfl_sync(0xffffffffu, w_lane, (t0 + b) & 31);
+        if (t0 + b < n_parts && w != 0.f) {
+          a.x = fmaf(w, x[b].x, a.x);
+          a.y = fmaf(w, x[b].y, a.y);
+          a.z = fmaf(w, x[b].z, a.z);
+          a.w = fmaf(w, x[b].w, a.w);
+        }
+      }
+    }
+    if (kBf16Out) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&lo);
+      pk.y = *reinterpret_cast<uint32_t*>(&hi);
+      reinterpret_cast<uint2*>(o)[row * 32 + lane] = pk;
+    } else {
+      reinterpret_cast<float4*>(o)[row * 32 + lane] = a;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_merge(int n_parts, int64_t rows, int d, const float* o_parts,
@@ -87,6 +135,15 @@ cudaError_t launch_merge(int n_parts, int64_t rows, int d, const float* o_parts,
   int64_t blocks = (rows + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)sms * 16;
   if (blocks > cap) blocks = cap;
+  if (d == 128 && n_parts <= 32) {
+    if (o_dtype == RA_DTYPE_BF16)
+      merge_d128_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(
+          n_parts, rows, reinterpret_cast<const float4*>(o_parts), lse_parts, o, lse);
+    else
+      merge_d128_kernel<false><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(
+          n_parts, rows, reinterpret_cast<const float4*>(o_parts), lse_parts, o, lse);
+    return cudaGetLastError();
+  }
   if (o_dtype == RA_DTYPE_BF16)
     merge_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(n_parts, rows, d, o_parts, lse_parts, o, lse);
   else
