@@ -49,6 +49,22 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, dist_mod, device):
+    """Element-wise maximum of per-rank values over all ranks (the values themselves
+    without a process group): the job is as slow as its slowest replica."""
+    if dist_mod is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world, flops_per_rank, ms):
+    """Whole-job TFLOP/s of `world` replicas that each do flops_per_rank in ms (weak scaling)."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -270,13 +286,10 @@ def run_ours(args, wl):
     fwd_ms = [e[1].elapsed_time(e[2]) for e in fwd_ev]
     perm_in_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in fwd_ev)
     perm_out_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in fwd_ev)
-    if pg is not None:
-        t = torch.tensor([total_ms, max(fwd_ms)], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms, fwd_max = t.tolist()
+    total_ms, fwd_max = max_over_ranks([total_ms, max(fwd_ms)], pg, dev)
     ms_per_step = total_ms / args.steps
     flops = wl.flops()
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_rate(world, flops, ms_per_step)
 
     # End to end through host buffers: every step copies its natural-order Q/K/V in
     # from pinned host memory and its O/LSE back out.  Steps are pipelined the way a
@@ -336,14 +349,10 @@ def run_ours(args, wl):
         run_pipeline(args.steps)
         e1.record(stream)
         barrier()
-        e_ms = e0.elapsed_time(e1) / args.steps
-        if pg is not None:
-            t = torch.tensor([e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e_ms = t.item()
+        e_ms = max_over_ranks([e0.elapsed_time(e1) / args.steps], pg, dev)[0]
         h2d_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h_bytes = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-        e2e = {"value": world * flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+        e2e = {"value": job_rate(world, flops, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                "note": "pinned host buffers, two device slots; H2D of step i+1 and D2H of step i-1 overlap step i"}
         ra.ra_sync_status(plan)
