@@ -2,9 +2,7 @@
 
 The rows are independent, so they are split over a process pool (``spawn``: a
 pool forked after CUDA initialisation can hang).  Each worker memory-maps the
-key/value head from a temporary float64 .npy file (in shared memory when the
-machine has /dev/shm) instead of receiving a copy; there is one task per worker,
-so each task reads the keys once for all of its rows.
+key/value head from a temporary .npy file instead of receiving a copy.
 """
 
 import multiprocessing as mp
@@ -26,26 +24,24 @@ def _init(kpath, vpath):
 def _work(args):
     import oracle
     q_rows, q_pos, causal, scale = args
-    return oracle.attention_rows(q_rows, _K, _V, q_positions=q_pos, causal=causal, scale=scale,
-                                 chunk=max(1, q_rows.shape[0]))
+    return oracle.attention_rows(q_rows, _K, _V, q_positions=q_pos, causal=causal, scale=scale)
 
 
-def attention_rows_parallel(q_rows, q_pos, k_head, v_head, causal, scale=None, workers=None):
+def attention_rows_parallel(q_rows, q_pos, k_head, v_head, causal, scale=None, workers=None, chunk=64):
     """oracle.attention_rows over natural-order keys, rows spread over processes."""
     q_rows = np.asarray(q_rows, np.float64)
     q_pos = np.asarray(q_pos, np.int64)
     n = q_rows.shape[0]
     workers = workers or min(16, os.cpu_count() or 1)
-    shm = "/dev/shm" if os.path.isdir("/dev/shm") and os.access("/dev/shm", os.W_OK) else None
-    tmp = tempfile.mkdtemp(prefix="ra_oracle_", dir=shm)
+    tmp = tempfile.mkdtemp(prefix="ra_oracle_")
     try:
         kpath, vpath = os.path.join(tmp, "k.npy"), os.path.join(tmp, "v.npy")
-        np.save(kpath, np.asarray(k_head, np.float64))
-        np.save(vpath, np.asarray(v_head, np.float64))
+        np.save(kpath, np.asarray(k_head, np.float32))
+        np.save(vpath, np.asarray(v_head, np.float32))
         order = np.argsort(q_pos, kind="stable")
         # interleave sorted rows so every task has a similar key range
         tasks, idx = [], []
-        n_tasks = max(1, min(workers, n))
+        n_tasks = max(1, min(workers * 4, (n + chunk - 1) // chunk))
         for t in range(n_tasks):
             sel = order[t::n_tasks]
             if sel.size:
