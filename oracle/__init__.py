@@ -41,7 +41,8 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
                             attention over the held block equals ``ring_partials`` entry t.
 ``attention_backward``      central finite differences of ``full_attention`` (float64) on tiny
                             cases, causal and not, with grouped heads; a single key gives
-                            dV = dO and dQ = dK = 0; the rows of dK sum to zero.
+                            dV = dO and dQ = dK = 0; the rows of dK sum to zero; row blocks
+                            give the same gradients as the whole.
 ``ring_backward``           equals ``attention_backward`` for every layout, causal and not.
 ``ulysses_seq_to_head``,    labelled rows land on the device of their head at their position;
 ``ulysses_head_to_seq``     the two exchanges are inverse; exchange, per-device attention,

@@ -36,11 +36,13 @@ def _mask(pos_q, pos_k, causal):
     return pos_k[None, :] <= pos_q[:, None]
 
 
-def attention_backward(q, k, v, do, causal=False, positions=None, scale=None):
+def attention_backward(q, k, v, do, causal=False, positions=None, scale=None, block=None):
     """dQ, dK, dV of O = attention(q, k, v) for the upstream gradient dO.
 
     q, do: [B, Hq, S, d]; k, v: [B, Hkv, S, d]; rows in any order when
     ``positions`` gives each row's natural position (default 0..S-1).
+    ``block``: take the query rows that many at a time (each row's softmax is its
+    own; dK and dV add the blocks' contributions), so long sequences fit in memory.
     Returns (dq [B, Hq, S, d], dk [B, Hkv, S, d], dv [B, Hkv, S, d]) in float64.
     """
     q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
@@ -52,22 +54,25 @@ def attention_backward(q, k, v, do, causal=False, positions=None, scale=None):
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
+    step = S if block is None else int(block)
     for b in range(B):
         for h in range(Hq):
             g = h // group
-            s = sc * (q[b, h] @ k[b, g].T)
-            if allowed is not None:
-                s = np.where(allowed, s, -np.inf)
-            s_max = s.max(axis=1, keepdims=True)
-            e = np.exp(s - s_max)
-            p = e / e.sum(axis=1, keepdims=True)
-            o = p @ v[b, g]
-            dp = do[b, h] @ v[b, g].T
-            delta = (do[b, h] * o).sum(axis=1, keepdims=True)
-            ds = p * (dp - delta)
-            dq[b, h] = sc * (ds @ k[b, g])
-            dk[b, g] += sc * (ds.T @ q[b, h])
-            dv[b, g] += p.T @ do[b, h]
+            for r0 in range(0, S, step):
+                rows = slice(r0, min(S, r0 + step))
+                s = sc * (q[b, h, rows] @ k[b, g].T)
+                if allowed is not None:
+                    s = np.where(allowed[rows], s, -np.inf)
+                s_max = s.max(axis=1, keepdims=True)
+                e = np.exp(s - s_max)
+                p = e / e.sum(axis=1, keepdims=True)
+                o = p @ v[b, g]
+                dp = do[b, h, rows] @ v[b, g].T
+                delta = (do[b, h, rows] * o).sum(axis=1, keepdims=True)
+                ds = p * (dp - delta)
+                dq[b, h, rows] = sc * (ds @ k[b, g])
+                dk[b, g] += sc * (ds.T @ q[b, h, rows])
+                dv[b, g] += p.T @ do[b, h, rows]
     return dq, dk, dv
 
 

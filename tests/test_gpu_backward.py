@@ -111,3 +111,28 @@ def test_f32_backward_matches_oracle(causal, layout):
     got, want = _run(2, 96, 4, 4, 4, layout, causal, seed=61, dtype="f32", d=32)
     for name, g_, w_ in zip(("dQ", "dK", "dV"), got, want):
         _close(to64(g_), w_, f"f32 {name}", rel_rms=1e-5, max_rel=F32_MAX_REL)
+
+
+def test_bf16_backward_32k_one_group():
+    """Full size: the 32k causal zigzag workload (32 query heads, 8 key/value heads);
+    the oracle recomputes one whole group -- key/value head 0 and query heads 0-3 --
+    so all 32768 rows of dK and dV and four heads of dQ are compared element by element."""
+    wl = workloads.WORKLOADS["causal_32k_n8"]
+    q, k, v = workloads.torch_inputs(wl, "cuda")
+    layout, n = "zigzag", wl.n_shards
+    ql, kl, vl = (ra.ra_layout_perm(t, layout, n) for t in (q, k, v))
+    del q, k, v
+    g = torch.Generator(device="cuda")
+    g.manual_seed(3232)
+    dol = torch.randn(ql.shape, generator=g, device="cuda").to(torch.bfloat16)
+    plan = ra.ra_plan(wl.batch, wl.seq, wl.heads_q, wl.heads_kv, wl.head_dim, n, layout, True, "bf16")
+    o, lse = ra.ra_fwd(plan, ql, kl, vl)
+    dq, dk, dv = ra.ra_bwd(plan, ql, kl, vl, o, lse, dol)
+    ra.ra_sync_status(plan)
+    G = wl.heads_q // wl.heads_kv
+    pos = oracle.layout_positions(layout, wl.seq, n)
+    want = oracle.attention_backward(to64(ql[:, :G]), to64(kl[:, :1]), to64(vl[:, :1]), to64(dol[:, :G]),
+                                     causal=True, positions=pos, block=2048)
+    for name, g_, w_ in zip(("dQ", "dK", "dV"), (dq[:, :G], dk[:, :1], dv[:, :1]), want):
+        err, rr = _close(to64(g_), w_, f"32k {name}")
+        print(f"32k {name}: max-abs {err:.2e} of max, rel-RMS {rr:.2e}")

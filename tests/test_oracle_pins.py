@@ -482,3 +482,14 @@ def test_ulysses_attention_equals_full():
     ow, lw = full_attention(ql, kl, vl, causal=True, positions=pos)
     np.testing.assert_allclose(o, ow, atol=1e-12)
     np.testing.assert_allclose(lse, lw, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_row_blocks(causal):
+    B, Hq, Hkv, S, d = 1, 4, 2, 40, 8
+    q, k, v, do = _rand((B, Hq, S, d), 120), _rand((B, Hkv, S, d), 121), _rand((B, Hkv, S, d), 122), _rand((B, Hq, S, d), 123)
+    pos = layout_positions(STRIPED, S, 4)
+    whole = oracle.attention_backward(q, k, v, do, causal=causal, positions=pos)
+    blocked = oracle.attention_backward(q, k, v, do, causal=causal, positions=pos, block=7)
+    for a, b in zip(whole, blocked):
+        np.testing.assert_allclose(b, a, atol=1e-13)
