@@ -20,24 +20,27 @@
 // is applied per element by global position (Module 23, "Exact by Construction").
 //
 // How (one persistent CTA per SM, 12 warps):
-//   warp 0     TMA producer: the item's two 128-row tiles (K, V in pass 0; Q, dO
-//              in pass 1) once, then 64-row tiles of the other two tensors (Q, dO
-//              and the tile's 64 LSE*log2(e) and D values in pass 0; K, V in pass 1)
-//              into a ring of stages.
-//   warp 1     tcgen05 issuer (converged warp, one elected lane):
-//              per streamed tile two SS MMAs (M = 128, N = 64) give the scores and
-//              dP (pass 0 transposed: keys are the TMEM lanes), then TS MMAs
-//              (M = 128, N = 128, K = 64) add P^T dO and dS^T Q (pass 0) or dS K
-//              (pass 1) into accumulators, reading P and dS from tensor memory and
-//              the streamed tile, still in shared memory, as an MN-major operand.
+//   warp 0     TMA producer: pass 0's own 128-row tiles (K, V) once per item, then
+//              64-row tiles of the streamed tensors (Q, dO and the tile's 64
+//              LSE*log2(e) and D values in pass 0; K, V in pass 1) into a ring of
+//              stages.
+//   warp 1     tcgen05 issuer (converged warp, one elected lane): per streamed tile
+//              two products (M = 128, N = 64) give the scores and dP -- SS in pass 0
+//              (keys are the TMEM lanes), TS in pass 1 with Q and dO read from tensor
+//              memory -- then TS products (M = 128, N = 128, K = 64) add P^T dO and
+//              dS^T Q (pass 0) or dS K (pass 1) into accumulators, reading P and dS
+//              from tensor memory and the streamed tile, still in shared memory, as
+//              an MN-major operand.
 //   warps 4-7 / 8-11  elementwise: one thread per TMEM lane turns scores and dP
 //              into P and dS (bf16, written back into tensor memory), for the
-//              even / odd streamed tiles; at the end of an item they write the
-//              accumulators (pass 0: warps 4-7 dV, 8-11 dK; pass 1: half of dQ each).
-// TMEM: tile buffers of 128 columns (scores 0-63, dP 64-127; P over 0-31 and dS
-// over 64-95 once computed) -- two in pass 0, whose accumulators dV and dK take
-// columns 256-511, three in pass 1, whose accumulator dQ takes 384-511 -- so that
-// the MMAs of the next tiles run while the elementwise warps work on earlier ones.
+//              even / odd streamed tiles; in pass 1 they first store the item's Q
+//              (warps 4-7) and dO (8-11) rows into tensor memory; at the end of an
+//              item they write the accumulators (pass 0: warps 4-7 dV, 8-11 dK;
+//              pass 1: half of dQ each).
+// TMEM: two tile buffers of 128 columns (scores 0-63, dP 64-127; P over 0-31 and
+// dS over 64-95 once computed), so the next tile's products run while the
+// elementwise warps work on the previous one; pass 0 keeps dV at 256 and dK at
+// 384, pass 1 dQ at 256, Q at 384 and dO at 448.
 // Every wait is bounded (~1 s); on expiry the CTA records it in the status word,
 // drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -57,7 +60,7 @@ constexpr uint32_t kRegsOther = 120;
 constexpr uint32_t kRegsCompute = 192;
 static_assert(128 * kRegsOther + 256 * kRegsCompute <= kThreads * kRegsLaunch, "register split");
 
-constexpr int kFixRows = 128;                     // rows of the item's own tiles
+constexpr int kFixRows = 128;                     // rows of an item's own tiles (a 128-row TMA box)
 constexpr int kStreamRows = 64;                   // rows of a streamed tile
 constexpr uint32_t kFixBytes = 128 * 128 * 2;     // one 128 x 128 bf16 tile
 constexpr uint32_t kFixHalf = 128 * 64 * 2;       // its 128-byte swizzle column
