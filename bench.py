@@ -508,10 +508,11 @@ def backward_report(ra, torch, plan, qkv, out, stream, flops, pg):
     b.record(stream)
     torch.cuda.synchronize()
     ra.ra_sync_status(plan)
-    ms = a.elapsed_time(b)
+    ms = max_over_ranks([a.elapsed_time(b)], pg, ql.device)[0]
     del dout, dq, dk, dv, scratch
-    return {"ms": ms, "TFLOP/s": 2.5 * flops / (ms * 1e-3) / 1e12,
-            "executed_TFLOP/s": 3.5 * flops / (ms * 1e-3) / 1e12,
+    world = dist_env()[0]
+    return {"ms": ms, "TFLOP/s": job_rate(world, 2.5 * flops, ms),
+            "executed_TFLOP/s": job_rate(world, 3.5 * flops, ms),
             "flops_convention": "2.5x forward (dV, dP, dQ, dK and the recomputed scores)",
             "launches": 3}
 
