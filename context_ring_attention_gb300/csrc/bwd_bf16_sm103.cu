@@ -48,7 +48,7 @@
 
 #include <cstdint>
 
-#include "ra_internal.h"
+#include "bwd_internal.h"
 #include "sm100_ptx.cuh"
 
 namespace ra {

@@ -16,7 +16,7 @@
 
 #include <cstdint>
 
-#include "ra_internal.h"
+#include "bwd_internal.h"
 
 namespace ra {
 namespace {

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "ra_internal.h"
+#include "bwd_internal.h"
 
 struct ra_plan_s {
   ra_problem prob;
