@@ -175,3 +175,25 @@ def test_ring_driver_f32_toy():
     ring, ring_lse = oracle.ring_sim(Q[None, None], K[None, None], V[None, None], 4)
     assert_f32_close(to64(o), ring, "toy O")
     assert_f32_close(to64(lse), ring_lse, "toy LSE")
+
+
+def test_round_synchronised_paths_match_fused():
+    # 131072 tokens take the round-synchronised schedule (cooperative launches) in the
+    # per-step, gathered and backward kernels too; each must agree with the fused
+    # ra_fwd (itself checked against the oracle at this size): the per-step partials
+    # bit for bit with ra_fwd's, the driver and the gathered forward within bf16
+    # rounding of the merge / visiting order.
+    B, S, Hq, Hkv, n, layout = 1, 131072, 4, 2, 8, "zigzag"
+    (q, k, v), _ = _inputs(B, S, Hq, Hkv, n, layout, seed=131)
+    plan = ra.ra_plan(B, S, Hq, Hkv, 128, n, layout, True, "bf16")
+    o, lse = ra.ra_fwd(plan, q, k, v)
+    op, lp = ra.ra_fwd(plan, q, k, v, partials=True)
+    o_parts = torch.empty_like(op)
+    lse_parts = torch.empty_like(lp)
+    o_r, lse_r = ra.ra_ring_fwd(plan, q, k, v, o_parts=o_parts, lse_parts=lse_parts)
+    k_all, v_all = ra.ra_allgather_kv(plan, k, v)
+    o_g, lse_g = ra.ra_fwd_gathered(plan, q, k_all, v_all)
+    ra.ra_sync_status(plan)
+    assert torch.equal(o_parts, op) and torch.equal(lse_parts, lp)
+    for what, (o_x, l_x) in (("ring driver", (o_r, lse_r)), ("gathered", (o_g, lse_g))):
+        assert_bf16_close(to64(o_x), to64(o), to64(l_x), to64(lse), f"{what} vs fused at 131k")

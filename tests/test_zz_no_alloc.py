@@ -64,3 +64,25 @@ def test_fwd_static_matches_fwd_on_two_calls():
         o_ref, lse_ref = ra.ra_fwd(plan, q, k, v)
         ra.ra_sync_status(plan)
         assert_bf16_close(to64(o), to64(o_ref), to64(lse), to64(lse_ref), f"static vs plan {layout}")
+
+
+@pytest.mark.gpu
+def test_fwd_static_round_synchronised():
+    # 131072 tokens: large enough for the round-synchronised schedule (cooperative
+    # launch); the static path builds the same work list, so it matches ra_fwd bit for bit
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    lib = ra.load_library()
+    B, S, Hq, Hkv, N, layout = 1, 131072, 4, 2, 8, "zigzag"
+    q, k, v = workloads.small_inputs(B, S, Hq, Hkv, 128, seed=99, device="cuda", dtype="bf16")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    prob = _problem(B, S, Hq, Hkv, N, layout, True)
+    stream = torch.cuda.current_stream()
+    st = lib.ra_fwd_static(ctypes.byref(prob), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
+    assert st == 0, ra.ra_last_error()
+    plan = ra.ra_plan(B, S, Hq, Hkv, 128, N, layout, True, "bf16")
+    o2, lse2 = ra.ra_fwd(plan, q, k, v)
+    ra.ra_sync_status(plan)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
