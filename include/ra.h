@@ -93,16 +93,21 @@ typedef struct ra_plan_s* ra_plan_t;
 
 /*
  * ra_plan -- validate a problem and build its ring schedule.
- * Builds, on the host, the list of query-tile work items in longest-first order
- * with the per-shard tile classification (FULL / PARTIAL / SKIP, see
- * ra_plan_tile_counts) and one list per ring step for ra_fwd_step; when a CUDA
- * device is current, it uploads the work tables, allocates the plan's device
- * status word and creates the three events ra_ring_fwd orders its streams with.  Without a device
- * the plan is host-only: tile counts work, ra_fwd returns RA_ERR_NO_DEVICE.
+ * Builds, on the host, the per-shard tile classification (FULL / PARTIAL / SKIP,
+ * see ra_plan_tile_counts) and, for BF16 problems, the work lists of the
+ * tensor-core kernels: the whole forward (ra_fwd), one list per ring step
+ * (ra_fwd_step), the gathered forward (ra_fwd_gathered) and the two backward
+ * passes (ra_bwd), each in longest-first order with key/value heads grouped.  It
+ * also picks each kernel's schedule: synchronised rounds when one key/value head's
+ * K and V exceed 32 MiB, otherwise items handed out as CTAs free up.  When a CUDA
+ * device is current, it uploads the work tables, allocates the plan's device status
+ * word and creates the three events ra_ring_fwd orders its streams with.  Without a
+ * device the plan is host-only: tile counts work, the compute calls return
+ * RA_ERR_NO_DEVICE.
  * *out receives the plan; release it with ra_plan_destroy.
  * Errors: RA_ERR_INVALID_ARG (null pointers, sizes < 1, S % N, zigzag S % 2N,
  * Hq % Hkv, bad enum), RA_ERR_UNSUPPORTED (BF16 with d != 128, F32 with d > 128,
- * more than 2^31 rows), RA_ERR_CUDA (device upload failed).
+ * more than 2^31 rows, more than 32767 shards), RA_ERR_CUDA (device upload failed).
  */
 ra_status ra_plan(const ra_problem* prob, ra_plan_t* out);
 
