@@ -43,6 +43,10 @@ Functions and what pins each one (tests in ``tests/test_oracle_pins.py``):
                             cases, causal and not, with grouped heads; a single key gives
                             dV = dO and dQ = dK = 0; the rows of dK sum to zero; row blocks
                             give the same gradients as the whole.
+``attention_backward_rows`` through ``attention_backward`` (which is built from it) the finite
+                            differences above; on its own, a subset of query rows gives
+                            those rows' dQ, and the key-row parts of all query rows split
+                            into subsets add up to dK and dV.
 ``ring_backward``           equals ``attention_backward`` for every layout, causal and not.
 ``ulysses_seq_to_head``,    labelled rows land on the device of their head at their position;
 ``ulysses_head_to_seq``     the two exchanges are inverse; exchange, per-device attention,
@@ -60,7 +64,7 @@ from .layouts import CONTIGUOUS, STRIPED, ZIGZAG, LAYOUTS, layout_positions, cau
 from .attention import attention_rows, full_attention, full_attention_rows
 from .ring import ring_sim, ring_partials, pass_blocks, held_blocks
 from .merge import merge_partials
-from .backward import attention_backward, ring_backward
+from .backward import attention_backward, attention_backward_rows, ring_backward
 from .ulysses import ulysses_seq_to_head, ulysses_head_to_seq
 from .tiles import tile_counts, tile_classes_bruteforce
 
@@ -69,6 +73,6 @@ __all__ = [
     "layout_positions", "causal_pair_counts", "to_natural",
     "full_attention", "full_attention_rows", "attention_rows",
     "ring_sim", "ring_partials", "pass_blocks", "held_blocks", "merge_partials",
-    "attention_backward", "ring_backward", "ulysses_seq_to_head", "ulysses_head_to_seq",
+    "attention_backward", "attention_backward_rows", "ring_backward", "ulysses_seq_to_head", "ulysses_head_to_seq",
     "tile_counts", "tile_classes_bruteforce",
 ]

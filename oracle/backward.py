@@ -36,6 +36,40 @@ def _mask(pos_q, pos_k, causal):
     return pos_k[None, :] <= pos_q[:, None]
 
 
+def attention_backward_rows(q_rows, do_rows, q_pos, k, v, k_pos=None, causal=False, scale=None, key_idx=None):
+    """The gradient terms owed to a set of query rows of one (batch, query head).
+
+    q_rows, do_rows: [n, d], the rows and their upstream gradients; q_pos: [n]
+    their positions.  k, v: [S, d], every key and value of the head's key/value
+    head, at positions ``k_pos`` (default 0..S-1).  A query row's dQ depends only
+    on its own row of P, so it comes out whole.  dK and dV are sums over query
+    rows: for the key rows ``key_idx`` (optional), the part these query rows add,
+    scale * dS[:, j]^T q_rows and P[:, j]^T do_rows.  The parts of every query row
+    that sees a key add up to that key's gradient.
+    Returns dq [n, d], and with ``key_idx`` also dk_part and dv_part [len(key_idx), d].
+    """
+    q_rows, do_rows = (np.asarray(t, dtype=np.float64) for t in (q_rows, do_rows))
+    k, v = np.asarray(k, dtype=np.float64), np.asarray(v, dtype=np.float64)
+    sc = _scale(q_rows.shape[1], scale)
+    kp = np.arange(k.shape[0], dtype=np.int64) if k_pos is None else np.asarray(k_pos, np.int64)
+    s = sc * (q_rows @ k.T)
+    allowed = _mask(np.asarray(q_pos, np.int64), kp, causal)
+    if allowed is not None:
+        s = np.where(allowed, s, -np.inf)
+    s_max = s.max(axis=1, keepdims=True)
+    e = np.exp(s - s_max)
+    p = e / e.sum(axis=1, keepdims=True)
+    o = p @ v
+    dp = do_rows @ v.T
+    delta = (do_rows * o).sum(axis=1, keepdims=True)
+    ds = p * (dp - delta)
+    dq = sc * (ds @ k)
+    if key_idx is None:
+        return dq
+    key_idx = np.asarray(key_idx, np.int64)
+    return dq, sc * (ds[:, key_idx].T @ q_rows), p[:, key_idx].T @ do_rows
+
+
 def attention_backward(q, k, v, do, causal=False, positions=None, scale=None, block=None):
     """dQ, dK, dV of O = attention(q, k, v) for the upstream gradient dO.
 
@@ -48,9 +82,8 @@ def attention_backward(q, k, v, do, causal=False, positions=None, scale=None, bl
     q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
     B, Hq, S, d = q.shape
     group = Hq // k.shape[1]
-    sc = _scale(d, scale)
     pos = np.arange(S, dtype=np.int64) if positions is None else np.asarray(positions, np.int64)
-    allowed = _mask(pos, pos, causal)
+    every_key = np.arange(S)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
@@ -60,19 +93,11 @@ def attention_backward(q, k, v, do, causal=False, positions=None, scale=None, bl
             g = h // group
             for r0 in range(0, S, step):
                 rows = slice(r0, min(S, r0 + step))
-                s = sc * (q[b, h, rows] @ k[b, g].T)
-                if allowed is not None:
-                    s = np.where(allowed[rows], s, -np.inf)
-                s_max = s.max(axis=1, keepdims=True)
-                e = np.exp(s - s_max)
-                p = e / e.sum(axis=1, keepdims=True)
-                o = p @ v[b, g]
-                dp = do[b, h, rows] @ v[b, g].T
-                delta = (do[b, h, rows] * o).sum(axis=1, keepdims=True)
-                ds = p * (dp - delta)
-                dq[b, h, rows] = sc * (ds @ k[b, g])
-                dk[b, g] += sc * (ds.T @ q[b, h, rows])
-                dv[b, g] += p.T @ do[b, h, rows]
+                dq[b, h, rows], dk_part, dv_part = attention_backward_rows(
+                    q[b, h, rows], do[b, h, rows], pos[rows], k[b, g], v[b, g], k_pos=pos, causal=causal,
+                    scale=scale, key_idx=every_key)
+                dk[b, g] += dk_part
+                dv[b, g] += dv_part
     return dq, dk, dv
 
 

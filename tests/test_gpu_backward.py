@@ -136,3 +136,76 @@ def test_bf16_backward_32k_one_group():
     for name, g_, w_ in zip(("dQ", "dK", "dV"), (dq[:, :G], dk[:, :1], dv[:, :1]), want):
         err, rr = _close(to64(g_), w_, f"32k {name}")
         print(f"32k {name}: max-abs {err:.2e} of max, rel-RMS {rr:.2e}")
+
+
+def test_bf16_backward_zigzag_1m_sampled():
+    """Full size, the way the benchmark runs it: the 1M-token causal zigzag workload,
+    ra_fwd then ra_bwd over the whole problem with the plan's own schedule.  What the
+    oracle can afford there:
+      * dQ of sampled query rows (a row's dQ needs only its own row of P), for the
+        query heads of key/value heads 0 and Hkv-1;
+      * dK and dV of the last 32 key positions of those two key/value heads: only
+        the last 32 query positions see them, so the oracle sums the parts of those
+        rows of the group's four query heads exactly (and checks their dQ too);
+      * for every key/value head, the rows of dV add up to the sum of the dO rows of
+        its query heads, because each row of P sums to one."""
+    wl = workloads.WORKLOADS["zigzag_1m_n8"]
+    layout, n, S = "zigzag", wl.n_shards, wl.seq
+    G = wl.heads_q // wl.heads_kv
+    q, k, v = workloads.torch_inputs(wl, "cuda")
+    ql, kl, vl = (ra.ra_layout_perm(t, layout, n) for t in (q, k, v))
+    del q, k, v
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4242)
+    dol = torch.randn(ql.shape, generator=g, device="cuda").to(torch.bfloat16)
+    plan = ra.ra_plan(wl.batch, S, wl.heads_q, wl.heads_kv, wl.head_dim, n, layout, True, "bf16")
+    o, lse = ra.ra_fwd(plan, ql, kl, vl)
+    dq, dk, dv = ra.ra_bwd(plan, ql, kl, vl, o, lse, dol)
+    ra.ra_sync_status(plan)
+    del o, lse
+
+    pos = oracle.layout_positions(layout, S, n)
+    row_of = np.empty(S, np.int64)
+    row_of[pos] = np.arange(S)                       # natural position -> layout row
+    nat = torch.from_numpy(row_of).cuda()
+
+    def rows(t, h, xs):                              # rows of head h at natural positions xs
+        return to64(t[0, h].index_select(0, torch.from_numpy(row_of[xs]).cuda()))
+
+    picks = np.asarray(workloads.sample_rows(wl, 256), np.int64)
+    tail = np.arange(S - 32, S)
+    got_dq, want_dq, got_kv, want_kv = [], [], [], []
+    for gk in (0, wl.heads_kv - 1):
+        kh = to64(kl[0, gk].index_select(0, nat))    # the group's keys and values, natural order
+        vh = to64(vl[0, gk].index_select(0, nat))
+        dk_tail, dv_tail = np.zeros((32, wl.head_dim)), np.zeros((32, wl.head_dim))
+        for h in range(gk * G, (gk + 1) * G):
+            dq_t, dk_p, dv_p = oracle.attention_backward_rows(rows(ql, h, tail), rows(dol, h, tail), tail, kh, vh,
+                                                              causal=True, key_idx=tail)
+            dk_tail += dk_p
+            dv_tail += dv_p
+            got_dq.append(rows(dq, h, tail))
+            want_dq.append(dq_t)
+            xs = picks[picks[:, 1] == h, 2]
+            for r0 in range(0, len(xs), 16):
+                blk = xs[r0:r0 + 16]
+                want_dq.append(oracle.attention_backward_rows(rows(ql, h, blk), rows(dol, h, blk), blk, kh, vh,
+                                                              causal=True))
+                got_dq.append(rows(dq, h, blk))
+        got_kv.append((rows(dk, gk, tail), rows(dv, gk, tail)))
+        want_kv.append((dk_tail, dv_tail))
+        del kh, vh
+    err, rr = _close(np.concatenate(got_dq), np.concatenate(want_dq), "1M sampled dQ")
+    print(f"1M dQ: {sum(len(x) for x in got_dq)} rows, max-abs {err:.2e} of max, rel-RMS {rr:.2e}")
+    for name, i in (("dK", 0), ("dV", 1)):
+        err, rr = _close(np.concatenate([x[i] for x in got_kv]), np.concatenate([x[i] for x in want_kv]),
+                         f"1M last-32 {name}")
+        print(f"1M last 32 keys {name}: max-abs {err:.2e} of max, rel-RMS {rr:.2e}")
+
+    # sum over keys of dV = sum over the group's query rows of dO (rows of P sum to one);
+    # rounding P to bf16 moves each row sum by about 2^-9, far inside 1e-2 of the total
+    for gk in range(wl.heads_kv):
+        got = dv[0, gk].float().cpu().numpy().sum(axis=0, dtype=np.float64)
+        want = sum(dol[0, h].float().cpu().numpy().sum(axis=0, dtype=np.float64) for h in range(gk * G, (gk + 1) * G))
+        rel = np.linalg.norm(got - want) / np.linalg.norm(want)
+        assert rel <= 1e-2, f"kv head {gk}: sum of dV rows off by {rel:.3e} of the dO sum"

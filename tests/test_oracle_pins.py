@@ -493,3 +493,60 @@ def test_backward_row_blocks(causal):
     blocked = oracle.attention_backward(q, k, v, do, causal=causal, positions=pos, block=7)
     for a, b in zip(whole, blocked):
         np.testing.assert_allclose(b, a, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_finite_differences(causal):
+    # L = sum over the chosen rows of O_i . dO_i, by central differences of attention_rows
+    S, d = 7, 3
+    q_rows, do_rows = _rand((3, d), 130), _rand((3, d), 131)
+    k, v = _rand((S, d), 132), _rand((S, d), 133)
+    q_pos = np.array([5, 2, 4])
+    key_idx = np.array([0, 2, 3, 5])
+    dq, dk_part, dv_part = oracle.attention_backward_rows(q_rows, do_rows, q_pos, k, v, causal=causal,
+                                                          key_idx=key_idx)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attention_rows(q_, k_, v_, q_positions=q_pos, causal=causal)
+        return float((o * do_rows).sum())
+
+    eps = 1e-6
+
+    def num_grad(x, f, rows):
+        g = np.zeros((len(rows), x.shape[1]))
+        for a, r in enumerate(rows):
+            for c in range(x.shape[1]):
+                xp, xm = x.copy(), x.copy()
+                xp[r, c] += eps
+                xm[r, c] -= eps
+                g[a, c] = (f(xp) - f(xm)) / (2 * eps)
+        return g
+
+    np.testing.assert_allclose(dq, num_grad(q_rows, lambda x: loss(x, k, v), range(3)), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dk_part, num_grad(k, lambda x: loss(q_rows, x, v), key_idx), atol=1e-7, rtol=1e-6)
+    np.testing.assert_allclose(dv_part, num_grad(v, lambda x: loss(q_rows, k, x), key_idx), atol=1e-7, rtol=1e-6)
+    if causal:   # keys after every chosen row get nothing
+        _, dk_late, dv_late = oracle.attention_backward_rows(q_rows, do_rows, q_pos, k, v, causal=True,
+                                                             key_idx=[S - 1])
+        assert np.all(dk_late == 0) and np.all(dv_late == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_subsets_add_up(causal):
+    # rows in a layout order, keys given by position; split the query rows into
+    # interleaved subsets: dQ rows match, and the key-row parts add up to dK, dV
+    B, Hq, Hkv, S, d = 1, 2, 1, 30, 4
+    q, k, v, do = _rand((B, Hq, S, d), 140), _rand((B, Hkv, S, d), 141), _rand((B, Hkv, S, d), 142), _rand((B, Hq, S, d), 143)
+    pos = layout_positions(ZIGZAG, S, 3)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, causal=causal, positions=pos)
+    keys = np.array([0, 7, 13, 29])
+    dk_sum, dv_sum = np.zeros((len(keys), d)), np.zeros((len(keys), d))
+    for h in range(Hq):
+        for sub in (np.arange(0, S, 3), np.arange(1, S, 3), np.arange(2, S, 3)):
+            dq_s, dk_p, dv_p = oracle.attention_backward_rows(q[0, h, sub], do[0, h, sub], pos[sub], k[0, 0], v[0, 0],
+                                                              k_pos=pos, causal=causal, key_idx=keys)
+            np.testing.assert_allclose(dq_s, dq[0, h, sub], atol=1e-13)
+            dk_sum += dk_p
+            dv_sum += dv_p
+    np.testing.assert_allclose(dk_sum, dk[0, 0, keys], atol=1e-12)
+    np.testing.assert_allclose(dv_sum, dv[0, 0, keys], atol=1e-12)
