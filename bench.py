@@ -65,6 +65,11 @@ def job_rate(world, flops_per_rank, ms):
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
+# A (batch, key/value head) unit of the end-to-end pipeline needs this many FLOPs
+# (about 0.1 s of forward) before a step is split into such units.
+E2E_UNIT_FLOPS = 2e14
+
+
 # ---------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -294,7 +299,11 @@ def run_ours(args, wl):
     # End to end through host buffers: every step copies its natural-order Q/K/V in
     # from pinned host memory and its O/LSE back out.  Steps are pipelined the way a
     # serving loop runs: step i+1's inputs travel (H2D stream) while step i computes,
-    # and step i's outputs travel back (D2H stream) while step i+1 computes.
+    # and step i's outputs travel back (D2H stream) while step i+1 computes.  When one
+    # (batch, key/value head) with its query heads is enough work to fill the GPU on
+    # its own (the 1M-token workload), a step also runs in such units: unit j's inputs
+    # arrive while unit j-1 computes and its outputs leave while unit j+1 computes, so
+    # that only the first unit's inputs and the last unit's outputs wait on the host link.
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
@@ -304,58 +313,107 @@ def run_ours(args, wl):
                 (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o_n),
                  torch.empty_like(lse_n))]
         h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        evs = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+        G = wl.heads_q // wl.heads_kv
+        if args.path == "fused" and wl.flops() / (wl.batch * wl.heads_kv) >= E2E_UNIT_FLOPS:
+            uplan = ra.ra_plan(1, wl.seq, G, 1, wl.head_dim, N, layout, wl.causal, wl.dtype)
+            units = [(b, g) for b in range(wl.batch) for g in range(wl.heads_kv)]
+        else:
+            uplan, units = None, [None]
+        U = len(units)
+
+        def qs(t, u):      # unit u's part of a [B, Hq, ...] tensor (a contiguous view)
+            return t if u is None else t[u[0]:u[0] + 1, u[1] * G:(u[1] + 1) * G]
+
+        def ks(t, u):      # ... of a [B, Hkv, ...] tensor
+            return t if u is None else t[u[0]:u[0] + 1, u[1]:u[1] + 1]
+
+        def unit_forward(u):
+            if u is None:
+                forward(ql, kl, vl)
+            else:
+                ra.ra_fwd(uplan, qs(ql, u), ks(kl, u), ks(vl, u), o=qs(o_l, u), lse=qs(lse_l, u))
+
+        evs = lambda: [[torch.cuda.Event() for _ in range(U)] for _ in range(2)]
         h2d_done, in_free, comp_done, d2h_done = evs(), evs(), evs(), evs()
 
-        def h2d(slot):
-            for t_h, t_d in zip((hq, hk, hv), bufs[slot][:3]):
-                t_d.copy_(t_h, non_blocking=True)
-            h2d_done[slot].record(h2d_s)
+        def h2d(slot, j):
+            u = units[j]
+            bq, bk, bv = bufs[slot][:3]
+            qs(bq, u).copy_(qs(hq, u), non_blocking=True)
+            ks(bk, u).copy_(ks(hk, u), non_blocking=True)
+            ks(bv, u).copy_(ks(hv, u), non_blocking=True)
+            h2d_done[slot][j].record(h2d_s)
 
-        def run_pipeline(n):
+        def run_pipeline(n, ev=None):
             with torch.cuda.stream(h2d_s):
-                h2d(0)
+                for j in range(U):
+                    h2d(0, j)
             for i in range(n):
                 b = i % 2
                 bq, bk, bv, bo, bl = bufs[b]
-                stream.wait_event(h2d_done[b])       # this step's inputs have arrived
-                ra.ra_layout_perm(bq, layout, N, out=ql)
-                ra.ra_layout_perm(bk, layout, N, out=kl)
-                ra.ra_layout_perm(bv, layout, N, out=vl)
-                in_free[b].record(stream)
-                forward(ql, kl, vl)
-                if i >= 2:
-                    stream.wait_event(d2h_done[b])   # step i-2's outputs have left this slot
-                ra.ra_layout_perm(o_l, layout, N, inverse=True, out=bo)
-                ra.ra_layout_perm(lse_l, layout, N, inverse=True, out=bl)
-                comp_done[b].record(stream)
-                if i + 1 < n:
-                    with torch.cuda.stream(h2d_s):
-                        if i >= 1:
-                            h2d_s.wait_event(in_free[1 - b])  # step i-1 has read its inputs
-                        h2d(1 - b)
-                with torch.cuda.stream(d2h_s):
-                    d2h_s.wait_event(comp_done[b])
-                    ho.copy_(bo, non_blocking=True)
-                    hl.copy_(bl, non_blocking=True)
-                    d2h_done[b].record(d2h_s)
+                for j, u in enumerate(units):
+                    stream.wait_event(h2d_done[b][j])     # this unit's inputs have arrived
+                    if ev is not None and j == 0:
+                        ev[i][0].record(stream)
+                    ra.ra_layout_perm(qs(bq, u), layout, N, out=qs(ql, u))
+                    ra.ra_layout_perm(ks(bk, u), layout, N, out=ks(kl, u))
+                    ra.ra_layout_perm(ks(bv, u), layout, N, out=ks(vl, u))
+                    in_free[b][j].record(stream)
+                    if ev is not None:
+                        ev[i][1 + 2 * j].record(stream)
+                    unit_forward(u)
+                    if ev is not None:
+                        ev[i][2 + 2 * j].record(stream)
+                    if i >= 2:
+                        stream.wait_event(d2h_done[b][j])  # step i-2's outputs have left this slot
+                    ra.ra_layout_perm(qs(o_l, u), layout, N, inverse=True, out=qs(bo, u))
+                    ra.ra_layout_perm(qs(lse_l, u), layout, N, inverse=True, out=qs(bl, u))
+                    comp_done[b][j].record(stream)
+                    if i + 1 < n:
+                        with torch.cuda.stream(h2d_s):
+                            if i >= 1:
+                                h2d_s.wait_event(in_free[1 - b][j])  # step i-1 has read these inputs
+                            h2d(1 - b, j)
+                    with torch.cuda.stream(d2h_s):
+                        d2h_s.wait_event(comp_done[b][j])
+                        qs(ho, u).copy_(qs(bo, u), non_blocking=True)
+                        qs(hl, u).copy_(qs(bl, u), non_blocking=True)
+                        d2h_done[b][j].record(d2h_s)
+                if ev is not None:
+                    ev[i][-1].record(stream)
             stream.wait_stream(h2d_s)
             stream.wait_stream(d2h_s)
 
         run_pipeline(2)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run_pipeline(args.steps)
-        e1.record(stream)
-        barrier()
+        e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * U)] for _ in range(args.steps)]
+        with ClockSampler(local) as e_clk:
+            e0.record(stream)
+            run_pipeline(args.steps, e_ev)
+            e1.record(stream)
+            barrier()
         e_ms = max_over_ranks([e0.elapsed_time(e1) / args.steps], pg, dev)[0]
+        # where the end-to-end time goes, on this rank
+        e_parts = {
+            "units_per_step": U,
+            "first_input_wait_ms": e0.elapsed_time(e_ev[0][0]),
+            "step_ms": statistics.mean(x[0].elapsed_time(x[-1]) for x in e_ev),
+            "fwd_ms": statistics.mean(sum(x[1 + 2 * j].elapsed_time(x[2 + 2 * j]) for j in range(U))
+                                      for x in e_ev),
+            "last_output_wait_ms": e_ev[-1][-1].elapsed_time(e1),
+        }
         h2d_bytes = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
         d2h_bytes = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
         e2e = {"value": job_rate(world, flops, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
-               "note": "pinned host buffers, two device slots; H2D of step i+1 and D2H of step i-1 overlap step i"}
+               "breakdown": e_parts, "clocks": e_clk.summary(),
+               "note": ("pinned host buffers, two device slots; H2D of step i+1 and D2H of step i-1 overlap "
+                        "step i" + ("; each step runs as one ra_fwd per (batch, key/value head) with its "
+                                    "query heads, whose copies overlap the neighbouring units" if U > 1 else ""))}
         ra.ra_sync_status(plan)
+        if uplan is not None:
+            ra.ra_sync_status(uplan)
 
     kernels = None
     if not args.no_kernels:
