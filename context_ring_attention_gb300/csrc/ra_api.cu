@@ -560,6 +560,7 @@ ra_status ra_layout_perm(int32_t layout, int64_t seq, int32_t n_shards, int32_t 
   if (s != RA_OK) return s;
   if (rows_outer < 1 || row_bytes < 4 || row_bytes % 4)
     return fail(RA_ERR_INVALID_ARG, "rows_outer >= 1 and row_bytes a positive multiple of 4 required");
+  if (rows_outer > INT64_MAX / seq / row_bytes) return fail(RA_ERR_UNSUPPORTED, "tensor above 2^63-1 bytes");
   if (src == nullptr || dst == nullptr) return fail(RA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_INVALID_ARG, "src/dst must be 16-byte aligned");
   const int64_t bytes = rows_outer * seq * (int64_t)row_bytes;
@@ -805,7 +806,7 @@ ra_status ra_ulysses_a2a(int32_t direction, int32_t layout, int64_t seq, int32_t
     return fail(RA_ERR_INVALID_ARG, "batch >= 1 and heads a positive multiple of n_shards required");
   if (row_bytes != 256 && row_bytes != 4)
     return fail(RA_ERR_UNSUPPORTED, "row_bytes must be 256 (d = 128 bf16) or 4 (one float)");
-  if (batch * (int64_t)heads * seq > INT32_MAX || batch > INT32_MAX)
+  if (batch > INT32_MAX || batch * (int64_t)heads * seq > INT32_MAX)
     return fail(RA_ERR_UNSUPPORTED, "B*H*S above 2^31-1 rows");
   if (src == nullptr || dst == nullptr) return fail(RA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_INVALID_ARG, "src/dst must be 16-byte aligned");

@@ -323,6 +323,7 @@ ra_status ra_merge_partials(int32_t n_parts, int64_t rows, int32_t d,
  * with pos the layout map above.  row_bytes must be a multiple of 4; pointers
  * 16-byte aligned; src and dst must not overlap.  Asynchronous; allocates nothing.
  * Errors: RA_ERR_INVALID_ARG (uneven shards, bad sizes, overlap, alignment),
+ * RA_ERR_UNSUPPORTED (seq above 2^31-1, n_shards above 32767, more than 2^63-1 bytes),
  * RA_ERR_CUDA.
  */
 ra_status ra_layout_perm(int32_t layout, int64_t seq, int32_t n_shards, int32_t inverse,

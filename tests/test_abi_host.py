@@ -85,6 +85,7 @@ def test_layout_perm_rejects_overlap_and_alignment(lib):
     assert lib.ra_layout_perm(0, 16, 2, 0, 1, 4, a, a + 16, None) == 1      # overlap
     assert lib.ra_layout_perm(0, 16, 2, 0, 1, 4, a + 4, a + 4096, None) == 1  # misaligned
     assert lib.ra_layout_perm(0, 16, 2, 0, 1, 6, a, a + 4096, None) == 1     # row_bytes % 4
+    assert lib.ra_layout_perm(0, 1 << 30, 2, 0, 1 << 40, 256, a, a + 4096, None) == 2  # size overflows
 
 
 @pytest.mark.parametrize("layout", oracle.LAYOUTS)
