@@ -44,8 +44,8 @@ def attention_backward_rows(q_rows, do_rows, q_pos, k, v, k_pos=None, causal=Fal
     head, at positions ``k_pos`` (default 0..S-1).  A query row's dQ depends only
     on its own row of P, so it comes out whole.  dK and dV are sums over query
     rows: for the key rows ``key_idx`` (optional), the part these query rows add,
-    scale * dS[:, j]^T q_rows and P[:, j]^T do_rows.  The parts of every query row
-    that sees a key add up to that key's gradient.
+    scale * dS[:, j]^T q_rows and P[:, j]^T do_rows (``key_idx`` may be a slice).
+    The parts of every query row that sees a key add up to that key's gradient.
     Returns dq [n, d], and with ``key_idx`` also dk_part and dv_part [len(key_idx), d].
     """
     q_rows, do_rows = (np.asarray(t, dtype=np.float64) for t in (q_rows, do_rows))
@@ -66,7 +66,8 @@ def attention_backward_rows(q_rows, do_rows, q_pos, k, v, k_pos=None, causal=Fal
     dq = sc * (ds @ k)
     if key_idx is None:
         return dq
-    key_idx = np.asarray(key_idx, np.int64)
+    if not isinstance(key_idx, slice):
+        key_idx = np.asarray(key_idx, np.int64)
     return dq, sc * (ds[:, key_idx].T @ q_rows), p[:, key_idx].T @ do_rows
 
 
@@ -83,7 +84,7 @@ def attention_backward(q, k, v, do, causal=False, positions=None, scale=None, bl
     B, Hq, S, d = q.shape
     group = Hq // k.shape[1]
     pos = np.arange(S, dtype=np.int64) if positions is None else np.asarray(positions, np.int64)
-    every_key = np.arange(S)
+    every_key = slice(None)
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
