@@ -22,7 +22,7 @@ __all__ = [
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
     "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
-    "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a",
+    "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a", "ra_wait_selftest",
     "library_path", "load_library", "EXPORTED",
 ]
 
@@ -33,7 +33,7 @@ _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
             "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
-            "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a")
+            "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a", "ra_wait_selftest")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -86,6 +86,7 @@ def load_library():
         "ra_allgather_kv": ([P, VP, VP, VP, VP, VP], I32),
         "ra_fwd_gathered": ([P, VP, VP, VP, VP, VP, VP], I32),
         "ra_ulysses_a2a": ([I32, I32, I64, I32, I64, I32, I32, VP, VP, VP], I32),
+        "ra_wait_selftest": ([VP], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -254,6 +255,14 @@ def ra_layout_index(layout, seq, n_shards):
     pos = np.zeros(int(seq), np.int64)
     _check(load_library().ra_layout_index(_layout(layout), int(seq), int(n_shards), pos.ctypes.data))
     return pos
+
+
+def ra_wait_selftest():
+    """Run the tensor-core kernels' bounded wait against a barrier nothing completes
+    (about one second); returns the status word it left (2: it gave up as designed)."""
+    word = ctypes.c_uint32(0)
+    _check(load_library().ra_wait_selftest(ctypes.addressof(word)))
+    return word.value
 
 
 def ra_sync_status(plan, stream=None):

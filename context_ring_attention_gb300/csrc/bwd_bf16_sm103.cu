@@ -145,6 +145,27 @@ __device__ __forceinline__ void drain_bar(const Ctl& c, uint32_t bar, uint32_t p
   }
 }
 
+// The bounded wait, run against a barrier that nothing completes: one warp
+// initialises an mbarrier for one arrival, never arrives, and waits for its first
+// phase.  The wait gives up after kWaitBudgetNs, records `who` in the status word and
+// returns, as in the tensor-core kernels when a handshake never comes.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t* status, uint32_t who) {
+  __shared__ __align__(8) uint64_t bar_word;
+  __shared__ uint32_t abort_flag;
+  const uint32_t bar = ptx::smem_addr(&bar_word);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar, 1);
+    abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  Ctl c;
+  c.bars = bar;
+  c.abort = &abort_flag;
+  c.status = status;
+  wait_bar(c, bar, 0u, who);
+}
+
 // ------------------------------------------------------------------- walks --
 // The streamed tiles of an item, in order.  Pass 0 (item = key tile of shard r
 // whose first key sits at position kmin): ring step t puts the block on shard
@@ -777,6 +798,11 @@ cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUte
 }
 
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t* status, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, kStatusTimeoutMma);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_bf16(int pass, const BwdParams& prm, const void* q, const void* k, const void* v,
                             const void* dout, int grid, cudaStream_t stream, const char** why) {

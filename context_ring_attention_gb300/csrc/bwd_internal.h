@@ -45,6 +45,9 @@ cudaError_t launch_bwd_f32(const BwdParams& prm, const float* q, const float* k,
 // pass 0: dK and dV (items are key tiles); pass 1: dQ (items are query tiles).
 cudaError_t launch_bwd_bf16(int pass, const BwdParams& prm, const void* q, const void* k, const void* v,
                             const void* dout, int grid, cudaStream_t stream, const char** why);
+// The tensor-core kernels' bounded wait on a barrier nothing completes (about 1 s);
+// it records kStatusTimeoutMma in *status.
+cudaError_t launch_wait_selftest(uint32_t* status, cudaStream_t stream);
 
 
 }  // namespace ra

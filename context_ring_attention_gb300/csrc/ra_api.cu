@@ -818,6 +818,24 @@ ra_status ra_ulysses_a2a(int32_t direction, int32_t layout, int64_t seq, int32_t
   return ok();
 }
 
+ra_status ra_wait_selftest(uint32_t* status_out) {
+  if (status_out == nullptr) return fail(RA_ERR_INVALID_ARG, "null status_out");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_NO_DEVICE, "no CUDA device");
+  }
+  uint32_t* d_word = nullptr;
+  cudaError_t e = cudaMalloc(&d_word, sizeof(uint32_t));
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+  e = cudaMemset(d_word, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = ra::launch_wait_selftest(d_word, nullptr);
+  if (e == cudaSuccess) e = cudaMemcpy(status_out, d_word, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  cudaFree(d_word);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "wait self-test: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 ra_status ra_sync_status(ra_plan_t plan, void* stream) {
   if (plan == nullptr) return fail(RA_ERR_INVALID_ARG, "null plan");
   if (plan->device < 0) return fail(RA_ERR_NO_DEVICE, "plan was built without a CUDA device");

@@ -375,6 +375,22 @@ ra_status ra_sync_status(ra_plan_t plan, void* stream);
 ra_status ra_fwd_static(const ra_problem* prob, const void* q, const void* k, const void* v,
                         void* o, float* lse, void* stream);
 
+/*
+ * ra_wait_selftest -- check the failure-detection path of the tensor-core kernels.
+ * Not a step of the method.  Every mbarrier wait in the tensor-core kernels gives
+ * up after about one second, records a bit in a device status word and lets its
+ * kernel return, so that a handshake that never comes ends in RA_ERR_TIMEOUT
+ * (ra_sync_status) instead of a hung GPU.  This call runs that wait routine once
+ * in a one-warp kernel against an mbarrier that nothing ever arrives on.
+ * *status_out (host) receives the status word the wait left: 2 (the MMA-side bit
+ * of ra_sync_status's message) when it gave up as designed, 0 if it never did.
+ * Later launches in the same context are unaffected.
+ * Synchronous, on the legacy default stream of the current device; it takes
+ * about one second.  It allocates one 4-byte device word and frees it.
+ * Errors: RA_ERR_INVALID_ARG (null status_out), RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ */
+ra_status ra_wait_selftest(uint32_t* status_out);
+
 /* Thread-local message describing the last failure on this thread ("" if none). */
 const char* ra_last_error(void);
 

@@ -50,6 +50,9 @@ def test_no_device_plan_refuses_fwd(lib):
     st = lib.ra_fwd(plan.handle, addr, addr, addr, addr, None, None, None, None)
     assert st == 5   # RA_ERR_NO_DEVICE
     assert "without a CUDA device" in ra.ra_last_error()
+    word = ctypes.c_uint32(7)
+    assert lib.ra_wait_selftest(ctypes.addressof(word)) == 5
+    assert word.value == 7
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -77,6 +80,7 @@ def test_null_arguments(lib):
     assert lib.ra_layout_perm(0, 8, 2, 0, 1, 4, None, None, None) == 1
     assert lib.ra_layout_index(0, 8, 3, None) == 1
     assert lib.ra_plan_destroy(None) == 0
+    assert lib.ra_wait_selftest(None) == 1
 
 
 def test_layout_perm_rejects_overlap_and_alignment(lib):

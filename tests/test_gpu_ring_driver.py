@@ -103,6 +103,39 @@ def test_step_equals_partials_and_oracle(case):
         assert np.all(to64(o_t)[~live] == 0)
 
 
+def test_any_ring_order_gives_the_same_answer():
+    """Module 23 ("The Math: One Block at a Time"): the fold does not depend on the order
+    in which the blocks arrive.  The shards visit their blocks in a shuffled step order,
+    one ra_fwd_step per step; merging the partials in that order gives the attention of
+    the oracle, and the in-order merge to within one bf16 rounding."""
+    B, S, Hq, Hkv, n, layout = 1, 2048, 8, 2, 4, "zigzag"
+    (q, k, v), pos = _inputs(B, S, Hq, Hkv, n, layout, seed=77)
+    plan = ra.ra_plan(B, S, Hq, Hkv, 128, n, layout, True, "bf16")
+    kb, vb = _bits(k), _bits(v)
+    parts = {}
+    for t in (2, 0, 3, 1):
+        kt = _from_bits(oracle.held_blocks(kb, n, t), k)
+        vt = _from_bits(oracle.held_blocks(vb, n, t), v)
+        parts[t] = ra.ra_fwd_step(plan, t, q, kt, vt)
+    ra.ra_sync_status(plan)
+    shuffled = [2, 0, 3, 1]
+    o_s, l_s = ra.ra_merge_partials(torch.stack([parts[t][0] for t in shuffled]).contiguous(),
+                                    torch.stack([parts[t][1] for t in shuffled]).contiguous(),
+                                    out_dtype=torch.bfloat16)
+    o_i, l_i = ra.ra_merge_partials(torch.stack([parts[t][0] for t in range(n)]).contiguous(),
+                                    torch.stack([parts[t][1] for t in range(n)]).contiguous(),
+                                    out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    ow, lw = oracle.full_attention(to64(q), to64(k), to64(v), causal=True, positions=pos)
+    assert_bf16_close(to64(o_s), ow, to64(l_s), lw, "shuffled ring order")
+    assert_bf16_close(to64(o_i), ow, to64(l_i), lw, "in-order ring")
+    # the two merges differ only in the order of fp32 additions (a few fp32 ulps of terms
+    # below 8 in magnitude), then each rounds to bf16 (half a step, 2^-8 relative)
+    a, b = to64(o_s), to64(o_i)
+    assert np.all(np.abs(a - b) <= 2.0 ** -7 * 1.01 * np.maximum(np.abs(a), np.abs(b)) + 4e-6)
+    assert np.abs(to64(l_s) - to64(l_i)).max() <= 1e-5
+
+
 def test_step_toy_ring_f32():
     # the Q&A page's toy ring: 4 devices x 3 tokens, d = 8, one step at a time
     wl = workloads.WORKLOADS["toy_ring_4x3_d8"]
