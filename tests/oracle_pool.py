@@ -2,7 +2,10 @@
 
 The rows are independent, so they are split over a process pool (``spawn``: a
 pool forked after CUDA initialisation can hang).  Each worker memory-maps the
-key/value head from a temporary .npy file instead of receiving a copy.
+key/value head from a temporary .npy file instead of receiving a copy, and runs
+its BLAS on one thread: one process per core already fills the machine, and a
+BLAS thread pool per process oversubscribes it (cores x cores threads), which was
+more than 20x slower.
 """
 
 import multiprocessing as mp
@@ -13,6 +16,7 @@ import tempfile
 import numpy as np
 
 _K = _V = None
+_BLAS_THREAD_VARS = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
 def _init(kpath, vpath):
@@ -48,8 +52,18 @@ def attention_rows_parallel(q_rows, q_pos, k_head, v_head, causal, scale=None, w
                 tasks.append((q_rows[sel], q_pos[sel], causal, scale))
                 idx.append(sel)
         ctx = mp.get_context("spawn")
-        with ctx.Pool(workers, initializer=_init, initargs=(kpath, vpath)) as pool:
-            res = pool.map(_work, tasks)
+        # spawned workers read the BLAS thread count from the environment at start-up
+        saved = {name: os.environ.get(name) for name in _BLAS_THREAD_VARS}
+        os.environ.update({name: "1" for name in _BLAS_THREAD_VARS})
+        try:
+            with ctx.Pool(workers, initializer=_init, initargs=(kpath, vpath)) as pool:
+                res = pool.map(_work, tasks)
+        finally:
+            for name, val in saved.items():
+                if val is None:
+                    os.environ.pop(name, None)
+                else:
+                    os.environ[name] = val
         out = np.zeros((n, q_rows.shape[1]))
         lse = np.full(n, -np.inf)
         for sel, (o, l) in zip(idx, res):
