@@ -75,7 +75,8 @@ int64_t build_items(const ra_problem& pb, int64_t* max_cost_out) {
   const bool head_pairs = ((pb.heads_q / pb.heads_kv) % 2) == 0;
   const int64_t per_shard = head_pairs ? (int64_t)n_qt * pb.batch * (pb.heads_q / 2)
                                        : (int64_t)((n_qt + 1) / 2) * pb.batch * pb.heads_q;
-  if (per_shard * N > kMaxItems) return -1;
+  // the list itself, and the costing below (every item against every ring step)
+  if (per_shard * N > kMaxItems || per_shard * N * N > (int64_t(1) << 30)) return -1;
   int64_t n = 0;
   for (int p = 0; p < N; ++p)
     for (int qt = 0; qt < n_qt; qt += head_pairs ? 1 : 2)
@@ -129,7 +130,8 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   std::lock_guard<std::mutex> lock(g_mutex);
   int64_t max_cost = 0;
   const int64_t n_items = build_items(*prob, &max_cost);
-  if (n_items < 0) return fail(RA_ERR_UNSUPPORTED, "work list exceeds the static maximum of 131072 items");
+  if (n_items < 0)
+    return fail(RA_ERR_UNSUPPORTED, "work list exceeds the static maximum of 131072 items (or 2^30 item-steps)");
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {

@@ -16,6 +16,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <exception>
 #include <new>
 #include <vector>
 
@@ -77,6 +78,9 @@ ra_status check_layout(int32_t layout, int64_t seq, int32_t n) {
   return RA_OK;
 }
 
+constexpr int64_t kMaxPlanPairs = int64_t(1) << 30;
+constexpr int64_t kMaxListEntries = int64_t(1) << 27;
+
 ra_status validate(const ra_problem* p) {
   if (p->batch < 1 || p->heads_q < 1 || p->heads_kv < 1 || p->head_dim < 1)
     return fail(RA_ERR_INVALID_ARG, "batch, heads and head_dim must be >= 1");
@@ -92,9 +96,23 @@ ra_status validate(const ra_problem* p) {
   } else {
     return fail(RA_ERR_INVALID_ARG, "unknown dtype %d", p->dtype);
   }
-  const int64_t rows = p->batch * (int64_t)p->heads_q * p->seq;
-  if (p->batch > INT32_MAX / p->heads_q || rows > INT32_MAX)
+  if (p->batch > INT32_MAX / p->heads_q || p->batch * (int64_t)p->heads_q * p->seq > INT32_MAX)
     return fail(RA_ERR_UNSUPPORTED, "B*Hq*S above 2^31-1 rows");
+  // The planner's own work: the tile classification visits N x n_qtiles x N
+  // (query tile, ring step) pairs, and the tensor-core work lists hold about
+  // n_items x (N + 2) entries.  Past these limits planning alone would take
+  // tens of seconds to hours and gigabytes of host memory.
+  const int64_t N = p->n_shards;
+  const int64_t n_qt = (p->seq / N + ra::kTileRows - 1) / ra::kTileRows;
+  if (N * N * n_qt > kMaxPlanPairs)
+    return fail(RA_ERR_UNSUPPORTED, "ring too large to plan: n_shards^2 x query tiles per shard above 2^30");
+  if (p->dtype == RA_DTYPE_BF16) {
+    const int G = p->heads_q / p->heads_kv;
+    const int64_t per_shard = (G % 2 == 0) ? n_qt * p->batch * (p->heads_q / 2)
+                                           : ((n_qt + 1) / 2) * p->batch * p->heads_q;
+    if (per_shard * N * (N + 2) > kMaxListEntries)
+      return fail(RA_ERR_UNSUPPORTED, "work lists too large to plan: items x (n_shards + 2) above 2^27");
+  }
   return RA_OK;
 }
 
@@ -471,7 +489,12 @@ ra_status ra_plan(const ra_problem* prob, ra_plan_t* out) {
   pl->prob = *prob;
   if (pl->prob.scale == 0.f) pl->prob.scale = 1.0f / std::sqrt((float)prob->head_dim);
   pl->s_n = prob->seq / prob->n_shards;
-  build_schedule(pl);
+  try {
+    build_schedule(pl);
+  } catch (const std::exception& ex) {  // host allocation of the work lists failed
+    delete pl;
+    return fail(RA_ERR_UNSUPPORTED, "planning failed on the host: %s", ex.what());
+  }
   s = upload(pl);
   if (s != RA_OK) {
     ra_plan_destroy(pl);

@@ -107,7 +107,9 @@ typedef struct ra_plan_s* ra_plan_t;
  * *out receives the plan; release it with ra_plan_destroy.
  * Errors: RA_ERR_INVALID_ARG (null pointers, sizes < 1, S % N, zigzag S % 2N,
  * Hq % Hkv, bad enum), RA_ERR_UNSUPPORTED (BF16 with d != 128, F32 with d > 128,
- * more than 2^31 rows, more than 32767 shards), RA_ERR_CUDA (device upload failed).
+ * more than 2^31 rows, more than 32767 shards; a plan too large to build on the
+ * host: N^2 x query tiles per shard above 2^30, BF16 work lists above 2^27
+ * entries, or a host allocation that failed), RA_ERR_CUDA (device upload failed).
  */
 ra_status ra_plan(const ra_problem* prob, ra_plan_t* out);
 
@@ -358,7 +360,8 @@ ra_status ra_sync_status(ra_plan_t plan, void* stream);
  *     array of 4 MiB + 256 B, held on every GPU that loads the library until the
  *     process exits.  Problems needing more than 131072 work items (one item per
  *     pair of 128-row query tiles; e.g. 1M tokens x 32 query heads is exactly
- *     131072) are rejected with RA_ERR_UNSUPPORTED.
+ *     131072), or more than 2^30 (item, ring step) pairs to cost, are rejected
+ *     with RA_ERR_UNSUPPORTED.
  *   - Set-up: the first call on a device (with that device current) looks up the
  *     array's device address; make that first call before any stream capture.
  *   - Sharing: every call reuses the array; the status word is cleared at the

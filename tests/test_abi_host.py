@@ -63,6 +63,9 @@ def test_no_device_plan_refuses_fwd(lib):
     (dict(dtype="f32", head_dim=256), 2),                           # f32 d <= 128
     (dict(batch=0), 1),
     (dict(scale=-1.0), 1),
+    # planner limits: N^2 x query tiles above 2^30; bf16 work lists above 2^27 entries
+    (dict(seq=32767 * 1024, n_shards=32767, heads_q=1, heads_kv=1), 2),
+    (dict(seq=4096 * 1024, n_shards=4096, heads_q=2, heads_kv=1), 2),
 ])
 def test_plan_rejects(lib, kw, status):
     args = dict(batch=1, seq=1024, heads_q=4, heads_kv=2, head_dim=128, n_shards=8, layout="contiguous",
