@@ -185,6 +185,21 @@ def _check_qkv(plan, **tensors):
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {(B, heads, S, d)}")
 
 
+def _need(name, t, shape, dtype, device):
+    """``t`` must be a contiguous tensor of exactly this shape and dtype on ``device``:
+    the library sees only its pointer, so a smaller buffer would be overrun."""
+    import torch
+    if (not isinstance(t, torch.Tensor) or tuple(t.shape) != tuple(int(x) for x in shape) or t.dtype != dtype
+            or not t.is_contiguous() or t.device != device):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+
+
+def _same_device(device, **tensors):
+    for name, t in tensors.items():
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {device}")
+
+
 def ra_fwd(plan, q, k, v, o=None, lse=None, partials=False, o_parts=None, lse_parts=None,
            stream=None):
     """Ring-attention forward.  Fused: returns (O, LSE).  partials=True: (O_parts, LSE_parts)."""
@@ -192,12 +207,15 @@ def ra_fwd(plan, q, k, v, o=None, lse=None, partials=False, o_parts=None, lse_pa
     pb = plan.problem
     B, Hq, S, d, N = pb["batch"], pb["heads_q"], pb["seq"], pb["head_dim"], pb["n_shards"]
     _check_qkv(plan, q=q, k=k, v=v)
+    _same_device(q.device, k=k, v=v)
     lib = load_library()
     if partials:
         if o_parts is None:
             o_parts = torch.empty((N, B, Hq, S, d), dtype=torch.float32, device=q.device)
         if lse_parts is None:
             lse_parts = torch.empty((N, B, Hq, S), dtype=torch.float32, device=q.device)
+        _need("o_parts", o_parts, (N, B, Hq, S, d), torch.float32, q.device)
+        _need("lse_parts", lse_parts, (N, B, Hq, S), torch.float32, q.device)
         _check(lib.ra_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), None, None, _ptr(o_parts),
                           _ptr(lse_parts), _stream(stream)))
         return o_parts, lse_parts
@@ -205,6 +223,8 @@ def ra_fwd(plan, q, k, v, o=None, lse=None, partials=False, o_parts=None, lse_pa
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _need("o", o, q.shape, q.dtype, q.device)
+    _need("lse", lse, (B, Hq, S), torch.float32, q.device)
     _check(lib.ra_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), None, None,
                       _stream(stream)))
     return o, lse
@@ -219,11 +239,18 @@ def ra_merge_partials(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stre
         raise ValueError("partials must be float32")
     if not (o_parts.is_contiguous() and lse_parts.is_contiguous()):
         raise ValueError("partials must be contiguous")
+    if tuple(lse_parts.shape) != tuple(o_parts.shape[:-1]):
+        raise ValueError("lse_parts must have the shape of o_parts without its last axis")
+    _same_device(o_parts.device, lse_parts=lse_parts)
     out_dtype = out_dtype or torch.float32
     if o is None:
         o = torch.empty(o_parts.shape[1:], dtype=out_dtype, device=o_parts.device)
     if lse is None:
         lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    if o.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("o must be float32 or bfloat16")
+    _need("o", o, o_parts.shape[1:], o.dtype, o_parts.device)
+    _need("lse", lse, lse_parts.shape[1:], torch.float32, o_parts.device)
     code = 1 if o.dtype == torch.bfloat16 else 0
     _check(load_library().ra_merge_partials(n, rows, d, _ptr(o_parts), _ptr(lse_parts), _ptr(o), code,
                                             _ptr(lse), _stream(stream)))
@@ -237,14 +264,15 @@ def ra_layout_perm(x, layout, n_shards, inverse=False, seq_dim=None, out=None, s
     [B, H, S] tensors.  Everything after the sequence axis moves as one row.
     """
     import torch
-    if not x.is_contiguous():
-        raise ValueError("x must be contiguous")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA tensor")
     seq_dim = (2 if seq_dim is None else seq_dim) % x.dim()
     seq = x.shape[seq_dim]
     outer = int(np.prod(x.shape[:seq_dim], dtype=np.int64)) if seq_dim else 1
     row_bytes = int(np.prod(x.shape[seq_dim + 1:], dtype=np.int64)) * x.element_size()
     if out is None:
         out = torch.empty_like(x)
+    _need("out", out, x.shape, x.dtype, x.device)
     _check(load_library().ra_layout_perm(_layout(layout), seq, int(n_shards), int(bool(inverse)), outer,
                                          row_bytes, _ptr(x), _ptr(out), _stream(stream)))
     return out
@@ -279,10 +307,17 @@ def ra_fwd_static(batch, seq, heads_q, heads_kv, n_shards, layout, causal, q, k,
     ``lse`` to avoid the two torch allocations this wrapper otherwise makes.
     """
     import torch
+    _need("q", q, (batch, heads_q, seq, 128), torch.bfloat16, q.device)
+    if not q.is_cuda:
+        raise ValueError("q must be a CUDA tensor")
+    _need("k", k, (batch, heads_kv, seq, 128), torch.bfloat16, q.device)
+    _need("v", v, (batch, heads_kv, seq, 128), torch.bfloat16, q.device)
     if o is None:
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((batch, heads_q, seq), dtype=torch.float32, device=q.device)
+    _need("o", o, q.shape, q.dtype, q.device)
+    _need("lse", lse, (batch, heads_q, seq), torch.float32, q.device)
     prob = _Problem(int(batch), int(seq), int(heads_q), int(heads_kv), 128, int(n_shards), _layout(layout),
                     int(bool(causal)), 1, float(scale or 0.0))
     _check(load_library().ra_fwd_static(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
@@ -300,10 +335,13 @@ def ra_fwd_step(plan, step, q, k_blk, v_blk, o_part=None, lse_part=None, stream=
     pb = plan.problem
     B, Hq, S, d = pb["batch"], pb["heads_q"], pb["seq"], pb["head_dim"]
     _check_qkv(plan, q=q, k_blk=k_blk, v_blk=v_blk)
+    _same_device(q.device, k_blk=k_blk, v_blk=v_blk)
     if o_part is None:
         o_part = torch.empty((B, Hq, S, d), dtype=torch.float32, device=q.device)
     if lse_part is None:
         lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _need("o_part", o_part, (B, Hq, S, d), torch.float32, q.device)
+    _need("lse_part", lse_part, (B, Hq, S), torch.float32, q.device)
     _check(load_library().ra_fwd_step(plan.handle, int(step), _ptr(q), _ptr(k_blk), _ptr(v_blk), _ptr(o_part),
                                       _ptr(lse_part), _stream(stream)))
     return o_part, lse_part
@@ -318,6 +356,7 @@ def ra_ring_rotate(plan, k_src, v_src, k_dst=None, v_dst=None, stream=None):
     if v_dst is None:
         v_dst = torch.empty_like(v_src)
     _check_qkv(plan, k_dst=k_dst, v_dst=v_dst)
+    _same_device(k_src.device, v_src=v_src, k_dst=k_dst, v_dst=v_dst)
     _check(load_library().ra_ring_rotate(plan.handle, _ptr(k_src), _ptr(v_src), _ptr(k_dst), _ptr(v_dst),
                                          _stream(stream)))
     return k_dst, v_dst
@@ -348,6 +387,14 @@ def ra_ring_fwd(plan, q, k, v, o=None, lse=None, k_buf=None, v_buf=None, o_parts
         o_parts = torch.empty((N, B, Hq, S, d), dtype=torch.float32, device=q.device)
     if lse_parts is None:
         lse_parts = torch.empty((N, B, Hq, S), dtype=torch.float32, device=q.device)
+    _same_device(q.device, k=k, v=v)
+    _need("o", o, q.shape, q.dtype, q.device)
+    _need("lse", lse, (B, Hq, S), torch.float32, q.device)
+    if N > 1:
+        _need("k_buf", k_buf, (2,) + tuple(k.shape), k.dtype, q.device)
+        _need("v_buf", v_buf, (2,) + tuple(v.shape), v.dtype, q.device)
+    _need("o_parts", o_parts, (N, B, Hq, S, d), torch.float32, q.device)
+    _need("lse_parts", lse_parts, (N, B, Hq, S), torch.float32, q.device)
     if comm_stream is None:
         comm_stream = torch.cuda.Stream(device=q.device)
     _check(load_library().ra_ring_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(k_buf),
@@ -376,10 +423,15 @@ def ra_bwd(plan, q, k, v, o, lse, dout, dq=None, dk=None, dv=None, scratch=None,
         dv = torch.empty_like(v)
     if scratch is None:
         scratch = torch.empty(ra_bwd_scratch_size(plan) // 4, dtype=torch.float32, device=q.device)
-    elif scratch.numel() * scratch.element_size() < ra_bwd_scratch_size(plan):
-        raise ValueError("scratch is smaller than ra_bwd_scratch_size(plan)")
-    if lse.dtype != torch.float32 or not lse.is_contiguous() or tuple(lse.shape) != (B, Hq, S):
-        raise ValueError("lse must be a contiguous float32 tensor of shape (B, Hq, S)")
+    elif (scratch.numel() * scratch.element_size() < ra_bwd_scratch_size(plan) or scratch.dtype != torch.float32
+          or not scratch.is_contiguous() or scratch.device != q.device):
+        raise ValueError("scratch must be a contiguous float32 tensor of at least ra_bwd_scratch_size(plan) "
+                         "bytes on the device of q")
+    _same_device(q.device, k=k, v=v, o=o, dout=dout)
+    _need("lse", lse, (B, Hq, S), torch.float32, q.device)
+    _need("dq", dq, q.shape, q.dtype, q.device)
+    _need("dk", dk, k.shape, k.dtype, q.device)
+    _need("dv", dv, v.shape, v.dtype, q.device)
     _check(load_library().ra_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(scratch), _stream(stream)))
     return dq, dk, dv
@@ -401,6 +453,7 @@ def ra_allgather_kv(plan, k, v, k_all=None, v_all=None, stream=None):
     if v_all is None:
         v_all = torch.empty_like(v)
     _check_qkv(plan, k_all=k_all, v_all=v_all)
+    _same_device(k.device, v=v, k_all=k_all, v_all=v_all)
     _check(load_library().ra_allgather_kv(plan.handle, _ptr(k), _ptr(v), _ptr(k_all), _ptr(v_all),
                                           _stream(stream)))
     return k_all, v_all
@@ -415,6 +468,9 @@ def ra_fwd_gathered(plan, q, k_all, v_all, o=None, lse=None, stream=None):
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((pb["batch"], pb["heads_q"], pb["seq"]), dtype=torch.float32, device=q.device)
+    _same_device(q.device, k_all=k_all, v_all=v_all)
+    _need("o", o, q.shape, q.dtype, q.device)
+    _need("lse", lse, (pb["batch"], pb["heads_q"], pb["seq"]), torch.float32, q.device)
     _check(load_library().ra_fwd_gathered(plan.handle, _ptr(q), _ptr(k_all), _ptr(v_all), _ptr(o), _ptr(lse),
                                           _stream(stream)))
     return o, lse
@@ -424,19 +480,24 @@ def ra_ulysses_a2a(x, layout, n_shards, direction, out=None, stream=None):
     """Ulysses' exchange.  direction 0: [B, H, S, ...] layout order -> [N, B, H/N, S, ...];
     direction 1: back.  Rows are d = 128 bf16 ([..., 128]) or one float32 ([...])."""
     import torch
-    if not x.is_contiguous():
-        raise ValueError("x must be contiguous")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError("x must be a contiguous CUDA tensor")
     N = int(n_shards)
     if direction == 0:
         B, H, S = x.shape[:3]
+        if N < 1 or H % N:
+            raise ValueError("the head count must be a multiple of n_shards")
         out_shape = (N, B, H // N, S) + tuple(x.shape[3:])
     else:
         n_, B, hl, S = x.shape[:4]
+        if n_ != N:
+            raise ValueError(f"x must have n_shards = {N} head shards on its first axis")
         H = hl * N
         out_shape = (B, H, S) + tuple(x.shape[4:])
     row_bytes = int(np.prod(x.shape[3 if direction == 0 else 4:], dtype=np.int64)) * x.element_size()
     if out is None:
         out = torch.empty(out_shape, dtype=x.dtype, device=x.device)
+    _need("out", out, out_shape, x.dtype, x.device)
     _check(load_library().ra_ulysses_a2a(int(direction), _layout(layout), int(S), N, int(B), int(H), row_bytes,
                                          _ptr(x), _ptr(out), _stream(stream)))
     return out

@@ -186,3 +186,18 @@ def test_bwd_scratch_size(lib):
     plan = ra.ra_plan(2, 900, 4, 2, 128, 3, "contiguous", True, "bf16")
     assert ra.ra_bwd_scratch_size(plan) == 2 * 4 * 3 * 5 * 128 * 4   # 300 rows per shard -> 5 blocks
     assert lib.ra_bwd_scratch_size(None, None) == 1
+
+
+def test_binding_buffer_check():
+    # the binding's check on caller buffers (shape, dtype, contiguity, device)
+    torch = pytest.importorskip("torch")
+    cpu = torch.device("cpu")
+    ra._need("t", torch.empty((2, 3, 4)), (2, 3, 4), torch.float32, cpu)
+    for bad in (torch.empty((2, 3, 5)), torch.empty((2, 3, 4), dtype=torch.bfloat16),
+                torch.empty((2, 4, 3)).transpose(1, 2), "not a tensor"):
+        with pytest.raises(ValueError):
+            ra._need("t", bad, (2, 3, 4), torch.float32, cpu)
+    with pytest.raises(ValueError):
+        ra._need("t", torch.empty((2, 3, 4)), (2, 3, 4), torch.float32, torch.device("cuda", 0))
+    with pytest.raises(ValueError):   # a CPU tensor never reaches the library
+        ra.ra_layout_perm(torch.empty((1, 1, 8, 4)), "contiguous", 2)
