@@ -201,3 +201,51 @@ def test_binding_buffer_check():
         ra._need("t", torch.empty((2, 3, 4)), (2, 3, 4), torch.float32, torch.device("cuda", 0))
     with pytest.raises(ValueError):   # a CPU tensor never reaches the library
         ra.ra_layout_perm(torch.empty((1, 1, 8, 4)), "contiguous", 2)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <stdint.h>
+#include "ra.h"
+
+int main(void) {
+  ra_problem p = {1, 32768, 32, 8, 128, 8, RA_LAYOUT_ZIGZAG, 1, RA_DTYPE_BF16, 0.0f};
+  ra_plan_t plan = NULL;
+  if (ra_plan(&p, &plan) != RA_OK) {
+    printf("plan: %s\n", ra_last_error());
+    return 1;
+  }
+  int64_t full[8], partial[8], skip[8];
+  if (ra_plan_tile_counts(plan, full, partial, skip) != RA_OK) return 2;
+  for (int i = 0; i < 8; ++i) printf("%lld %lld %lld\n", (long long)full[i], (long long)partial[i], (long long)skip[i]);
+  int64_t pos[16];
+  if (ra_layout_index(RA_LAYOUT_ZIGZAG, 16, 4, pos) != RA_OK) return 3;
+  for (int i = 0; i < 16; ++i) printf("%lld%c", (long long)pos[i], i == 15 ? '\n' : ' ');
+  ra_problem bad = p;
+  bad.seq = 100;
+  ra_plan_t none = NULL;
+  if (ra_plan(&bad, &none) != RA_ERR_INVALID_ARG || none != NULL) return 4;
+  printf("%s\n", ra_last_error());
+  return ra_plan_destroy(plan) == RA_OK ? 0 : 5;
+}
+"""
+
+
+def test_plain_c_caller(lib, tmp_path):
+    # the header compiles as C99 and the library links and runs from a C program
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(ra.library_path())
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), ra.library_path(), f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.splitlines()
+    want = oracle.tile_counts("zigzag", 32768, 8, causal=True)
+    got = np.array([[int(x) for x in ln.split()] for ln in out[:8]]).T
+    assert [g.tolist() for g in got] == [w.tolist() for w in want]
+    assert [int(x) for x in out[8].split()] == oracle.layout_positions("zigzag", 16, 4).tolist()
+    assert "multiple" in out[9] or "uneven" in out[9]
