@@ -161,9 +161,22 @@ CASES += [
      ["bwd_fd", "bwd_special"]),
     ("ring_bwd_probabilities_unnormalised", B_, "ring_backward", "p_blk = np.exp(s - lse[b, h, qp][:, None])",
      "p_blk = np.exp(s)", ["ring_bwd"]),
+    ("ring_bwd_group_overwrites", B_, "ring_backward", "dk[b, g, rows[r]] += dk_acc",
+     "dk[b, g, rows[r]] = dk_acc", ["ring_bwd"]),
     # Ulysses' exchange
     ("ulysses_keeps_layout_order", U, "ulysses_seq_to_head", "out[q, :, :, s] = x",
      "out[q, :, :, p * s_n + i] = x", ["ulysses_exchange", "ulysses_attention"]),
+    ("ulysses_back_in_natural_order", U, "ulysses_head_to_seq", "out[:, q * hl:(q + 1) * hl, p * s_n + i] = y",
+     "out[:, q * hl:(q + 1) * hl, s] = y", ["ulysses_exchange", "ulysses_attention"]),
+    # masks by position, exchanges by count, brute-force tile classes
+    ("mask_ignores_positions", A, "full_attention",
+     "pos = np.arange(S, dtype=np.int64) if positions is None else np.asarray(positions, np.int64)",
+     "pos = np.arange(S, dtype=np.int64)", ["rows_equal_full", "bwd_fd"]),
+    ("held_blocks_one_exchange_too_many", R, "held_blocks", "for _ in range(step):",
+     "for _ in range(step + 1):", ["pass_blocks", "held_partials"]),
+    ("brute_force_diagonal_dropped", T, "tile_classes_bruteforce",
+     "(kp[j0:j0 + tile][None, :] <= qp[i0:i0 + tile][:, None])",
+     "(kp[j0:j0 + tile][None, :] < qp[i0:i0 + tile][:, None])", ["tiles_brute_ragged", "tiles_brute_zigzag"]),
 ]
 
 
