@@ -510,6 +510,9 @@ ra_status ra_plan_destroy(ra_plan_t plan) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != plan->device) cudaSetDevice(plan->device);
+    // Kernels queued earlier on any stream may still read the work tables or the
+    // status word: let them finish before the memory goes back.
+    cudaDeviceSynchronize();
     cudaFree(plan->d_items);
     cudaFree(plan->d_step_items);
     cudaFree(plan->d_bwd_items);

@@ -113,7 +113,9 @@ typedef struct ra_plan_s* ra_plan_t;
  */
 ra_status ra_plan(const ra_problem* prob, ra_plan_t* out);
 
-/* Release a plan and its device memory.  NULL is accepted. */
+/* Release a plan and its device memory.  NULL is accepted.  It first waits for the
+ * plan's device to finish the work queued so far (which may still read the plan's
+ * tables), so it is synchronous; it does not clear a pending CUDA error. */
 ra_status ra_plan_destroy(ra_plan_t plan);
 
 /*
