@@ -1,12 +1,17 @@
-"""GB300 ring-attention forward: Python binding of libra.so (include/ra.h).
+"""GB300 ring attention -- forward, backward and the context-parallel variants:
+the Python binding of libra.so (include/ra.h).
 
-The functions keep the C names (``ra_plan``, ``ra_fwd``, ``ra_fwd_step``,
-``ra_ring_rotate``, ``ra_ring_fwd``, ``ra_bwd``, ``ra_merge_partials``, ``ra_layout_perm``,
-``ra_layout_index``, ``ra_plan_tile_counts``, ``ra_sync_status``,
-``ra_last_error``, ``ra_fwd_static``).  This module only marshals arguments:
-PyTorch supplies device memory and the current stream, every step of the
-computation runs in the library's CUDA kernels, and there is no fallback -- if
-libra.so is missing or cannot be loaded, every call raises.
+The functions keep the C names (``ra_plan``, ``ra_plan_tile_counts``, ``ra_fwd``,
+``ra_fwd_static``, ``ra_merge_partials``, ``ra_layout_perm``, ``ra_layout_index``,
+``ra_fwd_step``, ``ra_ring_rotate``, ``ra_ring_fwd``, ``ra_bwd``,
+``ra_bwd_scratch_size``, ``ra_allgather_kv``, ``ra_fwd_gathered``,
+``ra_ulysses_a2a``, ``ra_sync_status``, ``ra_wait_selftest``, ``ra_last_error``).
+This module only marshals arguments: PyTorch supplies device memory and the
+current stream, every step of the computation runs in the library's CUDA
+kernels, and there is no fallback -- if libra.so is missing or cannot be loaded,
+every call raises.  Because the library sees only pointers, every tensor a caller
+passes (outputs and scratch included) is checked here for its exact shape, dtype,
+contiguity and device before anything is launched.
 
 Tensors are ``[B, H, S, d]`` contiguous with S in layout order (shard p owns rows
 [p*S/N, (p+1)*S/N)); ``ra_layout_perm`` moves natural order <-> layout order.
