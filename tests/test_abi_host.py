@@ -120,6 +120,33 @@ def test_tile_counts_match_oracle(lib, layout, seq, n, causal):
         assert g.tolist() == w.tolist()
 
 
+def _random_problems(n_cases=60, seed=2024):
+    """Seeded (layout, seq, n_shards, causal) draws: ragged shards, odd N, tiny and long shards."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n_cases:
+        layout = ("contiguous", "striped", "zigzag")[rng.integers(3)]
+        n = int(rng.integers(1, 17))
+        unit = 2 * n if layout == "zigzag" else n
+        seq = unit * int(rng.integers(1, 4096 // unit + 1))
+        out.append((layout, seq, n, bool(rng.integers(2))))
+    return out
+
+
+@pytest.mark.parametrize("layout,seq,n,causal", _random_problems())
+def test_tile_counts_match_oracle_random(lib, layout, seq, n, causal):
+    plan = ra.ra_plan(1, seq, 2, 1, 128, n, layout, causal, "bf16")
+    got = ra.ra_plan_tile_counts(plan)
+    want = oracle.tile_counts(layout, seq, n, causal=causal, tile=128)
+    for g, w in zip(got, want):
+        assert g.tolist() == w.tolist()
+
+
+@pytest.mark.parametrize("layout,seq,n,causal", _random_problems(seed=2025))
+def test_layout_index_matches_oracle_random(lib, layout, seq, n, causal):
+    assert ra.ra_layout_index(layout, seq, n).tolist() == oracle.layout_positions(layout, seq, n).tolist()
+
+
 def test_tile_counts_seq32k_report():
     """The per-shard FULL/PARTIAL/SKIP table for 32768 tokens, 8 shards (reported by bench)."""
     for layout in ("contiguous", "zigzag"):
