@@ -1,18 +1,25 @@
-"""GPU parity at the full sizes of the benchmark workloads, on sampled rows.
+"""GPU parity at the full sizes of the benchmark workloads.
 
 Each workload runs exactly as bench.py runs it (natural-order inputs ->
-ra_layout_perm -> ra_fwd over the whole problem -> inverse ra_layout_perm), and
-the float64 oracle recomputes sampled rows one by one against every key.  The
-4096-token-per-shard 4k workload is also compared element by element on a few
-whole heads.
+ra_layout_perm -> ra_fwd over the whole problem -> inverse ra_layout_perm).
+* 4k non-causal (plain, and Q x4 on three seeds) and 32k causal (contiguous and
+  zigzag): every element of O and LSE of every (batch, query head) against the
+  float64 oracle, computed in full on all host cores.
+* 131k striped and 1M zigzag: 4096 sampled rows (forced edge rows plus uniform
+  draws, seed 7), each recomputed by the oracle against every key.
+The ring must equal ordinary attention everywhere (Module 23, "Exact by
+Construction"), so the full comparisons are the contract; the samples are what
+the float64 oracle can afford at the two largest sizes.
 """
+
+import dataclasses
 
 import numpy as np
 import pytest
 
 import oracle
-from tests.gpu_util import assert_bf16_close, to64
-from tests.oracle_pool import attention_rows_parallel
+from tests.gpu_util import BF16_MAX_ABS, assert_bf16_close, to64
+from tests.oracle_pool import attention_rows_parallel, full_attention_parallel
 
 torch = pytest.importorskip("torch")
 ra = pytest.importorskip("context_ring_attention_gb300")
@@ -68,22 +75,48 @@ def _check_sampled(wl, qkv, out, picks, what):
     print(f"{what}: {len(picks)} rows, O max-abs {err:.2e}, rel-RMS {rr:.2e}")
 
 
-@pytest.mark.parametrize("name", ["noncausal_4k_n8", "noncausal_4k_n8_q4"])
-def test_noncausal_4k(name):
-    wl = workloads.WORKLOADS[name]
-    plan, (q, k, v), (o, lse) = _run_workload(wl, "contiguous")
-    # two whole heads element by element
-    for h in (0, wl.heads_q - 1):
-        ow, lw = oracle.full_attention(to64(q[:1, h:h + 1]), to64(k[:1, h:h + 1]), to64(v[:1, h:h + 1]))
-        assert_bf16_close(to64(o[:1, h:h + 1]), ow, to64(lse[:1, h:h + 1]), lw, f"{name} head {h}")
-    _check_sampled(wl, (q, k, v), (o, lse), workloads.sample_rows(wl, 1024), name)
+def _check_full(wl, qkv, out, what, cache=None):
+    """Every element of O and LSE against the oracle computed in full (natural order)."""
+    q, k, v = qkv
+    o, lse = out
+    if cache is not None and wl.name in cache:
+        want_o, want_l = cache[wl.name]
+    else:
+        want_o, want_l = full_attention_parallel(q.float().cpu().numpy(), k.float().cpu().numpy(),
+                                                 v.float().cpu().numpy(), wl.causal)
+        if cache is not None:
+            cache[wl.name] = (want_o, want_l)
+    got_o, got_l = to64(o), to64(lse)
+    # the worst (batch, head) by max-abs error of O, and its margin to the bound
+    head_err = np.abs(got_o - want_o).max(axis=(2, 3))
+    b, h = np.unravel_index(int(np.argmax(head_err)), head_err.shape)
+    err, rr = assert_bf16_close(got_o, want_o, got_l, want_l, what)
+    print(f"{what}: all {wl.batch * wl.heads_q} heads in full, O max-abs {err:.3e} (worst head b={b} h={h}, "
+          f"{err / BF16_MAX_ABS:.0%} of the {BF16_MAX_ABS} bound), rel-RMS {rr:.2e}, "
+          f"LSE max-abs {np.abs(got_l - want_l).max():.2e}")
+    return err
+
+
+# The x4 variant is the one whose margin is tight (the bf16-rounded weights feed
+# the PV product; large logits make one or two keys dominate a row): three seeds.
+Q4_SEEDS = (2000, 2010, 2020)
+
+
+@pytest.mark.parametrize("name,seed", [("noncausal_4k_n8", 2000)] + [("noncausal_4k_n8_q4", s) for s in Q4_SEEDS])
+def test_noncausal_4k_full(name, seed):
+    wl = dataclasses.replace(workloads.WORKLOADS[name], seed_base=seed)
+    plan, qkv, out = _run_workload(wl, "contiguous")
+    _check_full(wl, qkv, out, f"{name} seed {seed}")
+
+
+_ORACLE_32K = {}  # both layouts share the natural-order inputs, hence one oracle result
 
 
 @pytest.mark.parametrize("layout", ["contiguous", "zigzag"])
-def test_causal_32k(layout):
+def test_causal_32k_full(layout):
     wl = workloads.WORKLOADS["causal_32k_n8"]
     plan, qkv, out = _run_workload(wl, layout)
-    _check_sampled(wl, qkv, out, workloads.sample_rows(wl, 1024), f"causal_32k {layout}")
+    _check_full(wl, qkv, out, f"causal_32k {layout}", cache=_ORACLE_32K)
     full, part, skip = ra.ra_plan_tile_counts(plan)
     want = oracle.tile_counts(layout, wl.seq, wl.n_shards, causal=True)
     assert [full.tolist(), part.tolist(), skip.tolist()] == [x.tolist() for x in want]
@@ -92,7 +125,7 @@ def test_causal_32k(layout):
 def test_striped_131k():
     wl = workloads.WORKLOADS["striped_131k_n32"]
     plan, qkv, out = _run_workload(wl, "striped")
-    _check_sampled(wl, qkv, out, workloads.sample_rows(wl, 1024), "striped_131k")
+    _check_sampled(wl, qkv, out, workloads.sample_rows(wl, 4096), "striped_131k")
 
 
 def test_zigzag_1m():
