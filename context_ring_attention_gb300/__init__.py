@@ -2,7 +2,7 @@
 the Python binding of libra.so (include/ra.h).
 
 The functions keep the C names (``ra_plan``, ``ra_plan_tile_counts``, ``ra_fwd``,
-``ra_fwd_static``, ``ra_merge_partials``, ``ra_layout_perm``, ``ra_layout_index``,
+``ra_fwd_static``, ``ra_fwd_static_status``, ``ra_merge_partials``, ``ra_layout_perm``, ``ra_layout_index``,
 ``ra_fwd_step``, ``ra_ring_rotate``, ``ra_ring_fwd``, ``ra_bwd``,
 ``ra_bwd_scratch_size``, ``ra_allgather_kv``, ``ra_fwd_gathered``,
 ``ra_ulysses_a2a``, ``ra_sync_status``, ``ra_wait_selftest``, ``ra_last_error``).
@@ -26,7 +26,7 @@ __all__ = [
     "RaError", "Plan", "LAYOUTS",
     "ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
     "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-    "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
+    "ra_fwd_static_status", "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
     "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a", "ra_wait_selftest",
     "library_path", "load_library", "EXPORTED",
 ]
@@ -37,7 +37,7 @@ _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_
            4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
-            "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
+            "ra_fwd_static_status", "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
             "ra_allgather_kv", "ra_fwd_gathered", "ra_ulysses_a2a", "ra_wait_selftest")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -83,6 +83,7 @@ def load_library():
         "ra_sync_status": ([P, VP], I32),
         "ra_last_error": ([], ctypes.c_char_p),
         "ra_fwd_static": ([ctypes.POINTER(_Problem), VP, VP, VP, VP, VP, VP], I32),
+        "ra_fwd_static_status": ([VP], I32),
         "ra_fwd_step": ([P, I32, VP, VP, VP, VP, VP, VP], I32),
         "ra_ring_rotate": ([P, VP, VP, VP, VP, VP], I32),
         "ra_ring_fwd": ([P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP], I32),
@@ -124,7 +125,22 @@ def _stream(stream):
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
+    cur = torch.cuda.current_device()
+    if stream.device.index != cur:
+        raise ValueError(f"the stream belongs to {stream.device}; the library launches on the current device "
+                         f"cuda:{cur}")
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on_current_device(name, t):
+    """The kernels run on the current CUDA device: every buffer must live there."""
+    import torch
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{cur} "
+                         f"(make its device current, e.g. with torch.cuda.device)")
 
 
 class Plan:
@@ -188,6 +204,7 @@ def _check_qkv(plan, **tensors):
         heads = pb["heads_q"] if name == "q" else pb["heads_kv"]
         if tuple(t.shape) != (B, heads, S, d) or t.dtype != dt or not t.is_contiguous() or not t.is_cuda:
             raise ValueError(f"{name} must be a contiguous CUDA {dt} tensor of shape {(B, heads, S, d)}")
+        _on_current_device(name, t)
 
 
 def _need(name, t, shape, dtype, device):
@@ -197,6 +214,7 @@ def _need(name, t, shape, dtype, device):
     if (not isinstance(t, torch.Tensor) or tuple(t.shape) != tuple(int(x) for x in shape) or t.dtype != dtype
             or not t.is_contiguous() or t.device != device):
         raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+    _on_current_device(name, t)
 
 
 def _same_device(device, **tensors):
@@ -246,6 +264,7 @@ def ra_merge_partials(o_parts, lse_parts, out_dtype=None, o=None, lse=None, stre
         raise ValueError("partials must be contiguous")
     if tuple(lse_parts.shape) != tuple(o_parts.shape[:-1]):
         raise ValueError("lse_parts must have the shape of o_parts without its last axis")
+    _on_current_device("o_parts", o_parts)
     _same_device(o_parts.device, lse_parts=lse_parts)
     out_dtype = out_dtype or torch.float32
     if o is None:
@@ -328,6 +347,12 @@ def ra_fwd_static(batch, seq, heads_q, heads_kv, n_shards, layout, causal, q, k,
     _check(load_library().ra_fwd_static(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                                         _stream(stream)))
     return o, lse
+
+
+def ra_fwd_static_status(stream=None):
+    """Raise RaError (RA_ERR_TIMEOUT) if the latest ra_fwd_static call on the current
+    device gave up on a device-side wait; synchronizes ``stream`` first."""
+    _check(load_library().ra_fwd_static_status(_stream(stream)))
 
 
 def ra_fwd_step(plan, step, q, k_blk, v_blk, o_part=None, lse_part=None, stream=None):

@@ -758,23 +758,10 @@ template <int kPass>
 cudaError_t launch_pass(const BwdParams& prm, const CUtensorMap& tx0, const CUtensorMap& tx1, const CUtensorMap& ty0,
                         const CUtensorMap& ty1, int grid, cudaStream_t stream, const char** why) {
   using C = Cfg<kPass>;
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, bwd_bf16_kernel<kPass>);
-  if (e != cudaSuccess) {
-    *why = "cudaFuncGetAttributes failed";
-    return e;
-  }
-  // setmaxnreg.inc waits until the registers exist: only launch when the split fits.
-  if ((uint32_t)attr.numRegs * kThreads < 128 * kRegsOther + 256 * kRegsCompute) {
-    *why = "kernel was built with fewer launch registers than its warpgroup split needs";
-    return cudaErrorInvalidConfiguration;
-  }
-  e = cudaFuncSetAttribute(bwd_bf16_kernel<kPass>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::kSmemBytes);
-  if (e != cudaSuccess) {
-    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-    return e;
-  }
+  static std::atomic<int> ready[kMaxDevices];
+  cudaError_t e = prepare_once(bwd_bf16_kernel<kPass>, ready, kThreads, 128 * kRegsOther + 256 * kRegsCompute,
+                               (int)C::kSmemBytes, why);
+  if (e != cudaSuccess) return e;
   if (prm.round_sync) {
     // The rounds wait on each other: a cooperative launch guarantees co-residency.
     cudaLaunchConfig_t cfg = {};

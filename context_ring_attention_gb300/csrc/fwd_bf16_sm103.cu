@@ -723,22 +723,10 @@ bool encode_rows(CUtensorMap* map, const void* base, int64_t rows) {
 template <bool kGathered>
 cudaError_t launch_kernel(const FwdParams& prm, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           int grid, cudaStream_t stream, const char** why) {
-  cudaFuncAttributes attr;
-  cudaError_t e = cudaFuncGetAttributes(&attr, fwd_bf16_kernel<kGathered>);
-  if (e != cudaSuccess) {
-    *why = "cudaFuncGetAttributes failed";
-    return e;
-  }
-  // setmaxnreg.inc waits until the registers exist: only launch when the split fits.
-  if ((uint32_t)attr.numRegs * kThreads < 128 * kRegsOther + 256 * kRegsSoftmax) {
-    *why = "kernel was built with fewer launch registers than its warpgroup split needs";
-    return cudaErrorInvalidConfiguration;
-  }
-  e = cudaFuncSetAttribute(fwd_bf16_kernel<kGathered>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  if (e != cudaSuccess) {
-    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-    return e;
-  }
+  static std::atomic<int> ready[kMaxDevices];
+  cudaError_t e = prepare_once(fwd_bf16_kernel<kGathered>, ready, kThreads, 128 * kRegsOther + 256 * kRegsSoftmax,
+                               (int)kSmemBytes, why);
+  if (e != cudaSuccess) return e;
   if (prm.round_sync) {
     // The rounds wait on each other: a cooperative launch guarantees that every CTA
     // is resident at once (it fails instead of starting otherwise).

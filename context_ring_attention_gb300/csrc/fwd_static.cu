@@ -26,7 +26,7 @@ namespace {
 constexpr int kMaxItems = 131072;           // work items: e.g. 1M tokens x 32 query heads
 constexpr size_t kStatusBytes = 256;        // status word at the start of the array
 constexpr size_t kScratchBytes = kStatusBytes + (size_t)kMaxItems * sizeof(ra::WorkItem);  // 4 MiB + 256 B
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = ra::kMaxDevices;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -65,45 +65,26 @@ ra_status check_problem(const ra_problem* p) {
   return RA_OK;
 }
 
-// The planner's work list (same items, same schedule order), written into
-// the static host buffer.  Returns the item count, or -1 when it would not fit;
-// *max_cost receives the longest item's key-tile count.
+// Whether the problem's work list fits the static arrays (and its costing, every
+// item against every ring step, stays short).
+bool fits(const ra_problem& pb) {
+  const int64_t N = pb.n_shards;
+  const int64_t items = ra::fwd_items_per_shard(pb, pb.seq / N) * N;
+  return items <= kMaxItems && items * N <= (int64_t(1) << 30);
+}
+
+// The planner's work list (ra::for_each_fwd_item, sorted by the same schedule
+// rule), written into the static host buffer.  Returns the item count, or -1 when
+// it would not fit; *max_cost receives the longest item's key-tile count.
 int64_t build_items(const ra_problem& pb, int64_t* max_cost_out) {
   const int N = pb.n_shards;
   const int64_t s_n = pb.seq / N;
-  const int n_qt = (int)((s_n + ra::kTileRows - 1) / ra::kTileRows);
-  const bool head_pairs = ((pb.heads_q / pb.heads_kv) % 2) == 0;
-  const int64_t per_shard = head_pairs ? (int64_t)n_qt * pb.batch * (pb.heads_q / 2)
-                                       : (int64_t)((n_qt + 1) / 2) * pb.batch * pb.heads_q;
-  // the list itself, and the costing below (every item against every ring step)
-  if (per_shard * N > kMaxItems || per_shard * N * N > (int64_t(1) << 30)) return -1;
+  if (!fits(pb)) return -1;
   int64_t n = 0;
-  for (int p = 0; p < N; ++p)
-    for (int qt = 0; qt < n_qt; qt += head_pairs ? 1 : 2)
-      for (int64_t b = 0; b < pb.batch; ++b)
-        for (int h = 0; h < pb.heads_q; h += head_pairs ? 2 : 1) {
-          ra::WorkItem w{};
-          w.bh0 = (int32_t)(b * pb.heads_q + h);
-          w.shard = p;
-          w.row0 = qt * ra::kTileRows;
-          if (head_pairs) {
-            w.bh1 = w.bh0 + 1;
-            w.row1 = w.row0;
-          } else if (qt + 1 < n_qt) {
-            w.bh1 = w.bh0;
-            w.row1 = w.row0 + ra::kTileRows;
-          } else {
-            w.bh1 = -1;
-            w.row1 = w.row0;
-          }
-          const int64_t top = std::min<int64_t>((w.bh1 >= 0 ? w.row1 : w.row0) + ra::kTileRows, s_n) - 1;
-          w.maxq = (int32_t)ra::pos_of(pb.layout, N, s_n, p, top);
-          int cost = 0;
-          for (int t = 0; t < N; ++t) cost += ra::visit_tiles(pb.layout, N, s_n, pb.causal, (p - t + N) % N, w.maxq);
-          w.cost = cost;
-          g_host_items[n] = {w, n};
-          ++n;
-        }
+  ra::for_each_fwd_item(pb, s_n, [&](const ra::WorkItem& w) {
+    g_host_items[n] = {w, n};
+    ++n;
+  });
   int64_t max_cost = 1;
   for (int64_t i = 0; i < n; ++i) max_cost = std::max<int64_t>(max_cost, g_host_items[i].w.cost);
   *max_cost_out = max_cost;
@@ -127,11 +108,14 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
   for (const void* p : ptrs)
     if (p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u)) return fail(RA_ERR_INVALID_ARG, "pointer not 16-byte aligned");
 
+  if (!fits(*prob))
+    return fail(RA_ERR_UNSUPPORTED, "work list exceeds the static maximum of 131072 items (or 2^30 item-steps)");
+  const ra_status dev_ok = ra::check_on_current_device(ptrs, 5, static_cast<cudaStream_t>(stream));
+  if (dev_ok != RA_OK) return dev_ok;
+
   std::lock_guard<std::mutex> lock(g_mutex);
   int64_t max_cost = 0;
   const int64_t n_items = build_items(*prob, &max_cost);
-  if (n_items < 0)
-    return fail(RA_ERR_UNSUPPORTED, "work list exceeds the static maximum of 131072 items (or 2^30 item-steps)");
 
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -199,7 +183,37 @@ extern "C" ra_status ra_fwd_static(const ra_problem* prob, const void* q, const 
     prm.round_sync = 0;
     e = ra::launch_fwd_bf16(prm, q, k, v, grid, st, &why);
   }
-  if (e != cudaSuccess) return fail(RA_ERR_CUDA, why);
+  if (e != cudaSuccess) {
+    char msg[200];
+    snprintf(msg, sizeof(msg), "%s: %s", why, cudaGetErrorString(e));
+    return fail(RA_ERR_CUDA, msg);
+  }
+  ra::set_last_error("");
+  return RA_OK;
+}
+
+extern "C" ra_status ra_fwd_static_status(void* stream) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_NO_DEVICE, "no CUDA device");
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (dev < 0 || dev >= kMaxDevices || g_dev_addr[dev] == nullptr) {  // no call on this device yet
+    ra::set_last_error("");
+    return RA_OK;
+  }
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  uint32_t word = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&word, g_dev_addr[dev], sizeof(word), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && word != 0) e = cudaMemset(g_dev_addr[dev], 0, sizeof(word));
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, cudaGetErrorString(e));
+  if (word != 0) {
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "device wait ran out of budget (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 teardown)", word);
+    return fail(RA_ERR_TIMEOUT, msg);
+  }
   ra::set_last_error("");
   return RA_OK;
 }

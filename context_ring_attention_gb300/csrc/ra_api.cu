@@ -42,9 +42,21 @@ struct ra_plan_s {
   ra::WorkItem* d_bwd_items = nullptr;
   ra::WorkItem* d_gather_items = nullptr;
   uint32_t* d_status = nullptr;
+  // Stream of the plan's own allocations: its device tables are allocated and freed
+  // in stream order on it (cudaMallocAsync / cudaFreeAsync), so that destroying a plan
+  // never waits on the host for the device.
+  cudaStream_t mem_stream = nullptr;
   cudaEvent_t ev_entry = nullptr, ev_rot = nullptr, ev_step = nullptr;  // ra_ring_fwd ordering
   bool round_sync = false;  // forward kernel schedule (ra::use_round_sync)
   int sm_count = 0;
+  // One event per stream the plan's kernels were queued on, recorded after the
+  // latest of them: ra_plan_destroy waits for exactly this work before it frees the
+  // device tables.  A slot whose event has completed is reused for a new stream.
+  struct StreamMark {
+    cudaStream_t stream;
+    cudaEvent_t done;
+  };
+  std::vector<StreamMark> marks;
 };
 
 namespace {
@@ -107,9 +119,7 @@ ra_status validate(const ra_problem* p) {
   if (N * N * n_qt > kMaxPlanPairs)
     return fail(RA_ERR_UNSUPPORTED, "ring too large to plan: n_shards^2 x query tiles per shard above 2^30");
   if (p->dtype == RA_DTYPE_BF16) {
-    const int G = p->heads_q / p->heads_kv;
-    const int64_t per_shard = (G % 2 == 0) ? n_qt * p->batch * (p->heads_q / 2)
-                                           : ((n_qt + 1) / 2) * p->batch * p->heads_q;
+    const int64_t per_shard = ra::fwd_items_per_shard(*p, p->seq / N);
     if (per_shard * N * (N + 2) > kMaxListEntries)
       return fail(RA_ERR_UNSUPPORTED, "work lists too large to plan: items x (n_shards + 2) above 2^27");
   }
@@ -265,38 +275,9 @@ void build_schedule(ra_plan_s* pl) {
   if (pb.dtype != RA_DTYPE_BF16) return;  // the SIMT kernel walks rows, not items
 
   const int G = pb.heads_q / pb.heads_kv;
-  const bool head_pairs = (G % 2) == 0;
   std::vector<Keyed> list;
   int64_t seqno = 0;
-  for (int p = 0; p < N; ++p) {
-    for (int qt = 0; qt < pl->n_qtiles; qt += head_pairs ? 1 : 2) {
-      for (int64_t b = 0; b < pb.batch; ++b) {
-        for (int h = 0; h < pb.heads_q; h += head_pairs ? 2 : 1) {
-          ra::WorkItem w{};
-          w.bh0 = (int32_t)(b * pb.heads_q + h);
-          w.shard = p;
-          w.row0 = qt * ra::kTileRows;
-          if (head_pairs) {
-            w.bh1 = w.bh0 + 1;
-            w.row1 = w.row0;
-          } else if (qt + 1 < pl->n_qtiles) {
-            w.bh1 = w.bh0;
-            w.row1 = w.row0 + ra::kTileRows;
-          } else {
-            w.bh1 = -1;
-            w.row1 = w.row0;
-          }
-          const int64_t top_row = (w.bh1 >= 0) ? w.row1 : w.row0;
-          w.maxq = (int32_t)last_row_pos(pb, s_n, p, top_row);
-          int cost = 0;
-          for (int t = 0; t < N; ++t)
-            cost += ra::visit_tiles(pb.layout, N, s_n, pb.causal, (p - t + N) % N, w.maxq);
-          w.cost = cost;
-          list.push_back({w, seqno++});
-        }
-      }
-    }
-  }
+  ra::for_each_fwd_item(pb, s_n, [&](const ra::WorkItem& w) { list.push_back({w, seqno++}); });
   pl->items = schedule(list, pb.heads_q, G);
   int64_t max_cost = 0;
   for (const Keyed& k : list) max_cost = std::max<int64_t>(max_cost, k.w.cost);
@@ -347,32 +328,26 @@ ra_status upload(ra_plan_s* pl) {
   }
   pl->device = dev;
   cudaDeviceGetAttribute(&pl->sm_count, cudaDevAttrMultiProcessorCount, dev);
-  cudaError_t e = cudaMalloc(&pl->d_status, 256);
-  if (e == cudaSuccess) e = cudaMemset(pl->d_status, 0, 256);
-  if (e == cudaSuccess && !pl->items.empty()) {
-    e = cudaMalloc(&pl->d_items, pl->items.size() * sizeof(ra::WorkItem));
-    if (e == cudaSuccess)
-      e = cudaMemcpy(pl->d_items, pl->items.data(), pl->items.size() * sizeof(ra::WorkItem),
-                     cudaMemcpyHostToDevice);
+  cudaError_t e = cudaStreamCreateWithFlags(&pl->mem_stream, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    pl->mem_stream = nullptr;
+    return fail(RA_ERR_CUDA, "plan stream: %s", cudaGetErrorString(e));
   }
-  if (e == cudaSuccess && !pl->step_items.empty()) {
-    e = cudaMalloc(&pl->d_step_items, pl->step_items.size() * sizeof(ra::WorkItem));
-    if (e == cudaSuccess)
-      e = cudaMemcpy(pl->d_step_items, pl->step_items.data(), pl->step_items.size() * sizeof(ra::WorkItem),
-                     cudaMemcpyHostToDevice);
-  }
-  if (e == cudaSuccess && !pl->bwd_items.empty()) {
-    e = cudaMalloc(&pl->d_bwd_items, pl->bwd_items.size() * sizeof(ra::WorkItem));
-    if (e == cudaSuccess)
-      e = cudaMemcpy(pl->d_bwd_items, pl->bwd_items.data(), pl->bwd_items.size() * sizeof(ra::WorkItem),
-                     cudaMemcpyHostToDevice);
-  }
-  if (e == cudaSuccess && !pl->gather_items.empty()) {
-    e = cudaMalloc(&pl->d_gather_items, pl->gather_items.size() * sizeof(ra::WorkItem));
-    if (e == cudaSuccess)
-      e = cudaMemcpy(pl->d_gather_items, pl->gather_items.data(), pl->gather_items.size() * sizeof(ra::WorkItem),
-                     cudaMemcpyHostToDevice);
-  }
+  cudaStream_t ms = pl->mem_stream;
+  e = cudaMallocAsync(reinterpret_cast<void**>(&pl->d_status), 256, ms);
+  if (e == cudaSuccess) e = cudaMemsetAsync(pl->d_status, 0, 256, ms);
+  auto put = [&](const std::vector<ra::WorkItem>& host, ra::WorkItem** dev) {
+    if (e != cudaSuccess || host.empty()) return;
+    const size_t bytes = host.size() * sizeof(ra::WorkItem);
+    e = cudaMallocAsync(reinterpret_cast<void**>(dev), bytes, ms);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(*dev, host.data(), bytes, cudaMemcpyHostToDevice, ms);
+  };
+  put(pl->items, &pl->d_items);
+  put(pl->step_items, &pl->d_step_items);
+  put(pl->bwd_items, &pl->d_bwd_items);
+  put(pl->gather_items, &pl->d_gather_items);
+  // the tables are in place before any launch on another stream reads them
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ms);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_entry, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_rot, cudaEventDisableTiming);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&pl->ev_step, cudaEventDisableTiming);
@@ -408,8 +383,10 @@ ra::FwdParams fwd_params(const ra_plan_s* plan) {
   return prm;
 }
 
+ra_status mark_use(ra_plan_s* plan, cudaStream_t st);
+
 // Launch the plan's forward kernel (tensor-core for bf16, SIMT for f32) on stream.
-ra_status launch(const ra_plan_s* plan, const ra::FwdParams& prm, const void* q, const void* k,
+ra_status launch(ra_plan_s* plan, const ra::FwdParams& prm, const void* q, const void* k,
                  const void* v, cudaStream_t st) {
   cudaError_t e;
   if (plan->prob.dtype == RA_DTYPE_BF16) {
@@ -434,7 +411,8 @@ ra_status launch(const ra_plan_s* plan, const ra::FwdParams& prm, const void* q,
                            static_cast<const float*>(v), st);
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "f32 forward launch failed: %s", cudaGetErrorString(e));
   }
-  return ok();
+  const ra_status s = mark_use(plan, st);
+  return s != RA_OK ? s : ok();
 }
 
 ra_status check_device(const ra_plan_s* plan) {
@@ -442,6 +420,35 @@ ra_status check_device(const ra_plan_s* plan) {
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != plan->device)
     return fail(RA_ERR_INVALID_ARG, "current device %d differs from the plan's device %d", cur, plan->device);
+  return RA_OK;
+}
+
+// Record, on `st`, that the plan's device tables are in use by the work queued there
+// so far (ra_plan_destroy waits for it).
+ra_status mark_use(ra_plan_s* plan, cudaStream_t st) {
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) cudaGetLastError();
+  if (cap != cudaStreamCaptureStatusNone) return RA_OK;  // queued into a graph, not run yet
+  ra_plan_s::StreamMark* slot = nullptr;
+  for (ra_plan_s::StreamMark& m : plan->marks)
+    if (m.stream == st) slot = &m;
+  if (slot == nullptr)
+    for (ra_plan_s::StreamMark& m : plan->marks)
+      if (cudaEventQuery(m.done) == cudaSuccess) {  // that stream's use has ended
+        m.stream = st;
+        slot = &m;
+        break;
+      }
+  cudaGetLastError();  // a not-ready query is not an error
+  if (slot == nullptr) {
+    cudaEvent_t ev = nullptr;
+    const cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) return fail(RA_ERR_CUDA, "plan use event: %s", cudaGetErrorString(e));
+    plan->marks.push_back({st, ev});
+    slot = &plan->marks.back();
+  }
+  const cudaError_t e = cudaEventRecord(slot->done, st);
+  if (e != cudaSuccess) return fail(RA_ERR_CUDA, "plan use event record: %s", cudaGetErrorString(e));
   return RA_OK;
 }
 
@@ -477,6 +484,38 @@ cudaError_t rotate_one(const ra_plan_s* plan, const void* src, void* dst, cudaSt
 
 void ra::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
 
+ra_status ra::check_on_current_device(const void* const* ptrs, int n, cudaStream_t stream) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_NO_DEVICE, "no CUDA device");
+  }
+  for (int i = 0; i < n; ++i) {
+    if (ptrs[i] == nullptr) continue;
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, ptrs[i]);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(RA_ERR_INVALID_ARG, "pointer %p: %s", ptrs[i], cudaGetErrorString(e));
+    }
+    if (a.type == cudaMemoryTypeDevice) {
+      if (a.device != cur)
+        return fail(RA_ERR_INVALID_ARG, "pointer %p is memory of device %d, the current device is %d", ptrs[i],
+                    a.device, cur);
+    } else if (a.type != cudaMemoryTypeManaged) {
+      return fail(RA_ERR_INVALID_ARG, "pointer %p is not device memory", ptrs[i]);
+    }
+  }
+  int sd = -1;
+  const cudaError_t e = cudaStreamGetDevice(stream, &sd);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(RA_ERR_INVALID_ARG, "stream: %s", cudaGetErrorString(e));
+  }
+  if (sd != cur) return fail(RA_ERR_INVALID_ARG, "the stream belongs to device %d, the current device is %d", sd, cur);
+  return RA_OK;
+}
+
 extern "C" {
 
 ra_status ra_plan(const ra_problem* prob, ra_plan_t* out) {
@@ -485,7 +524,7 @@ ra_status ra_plan(const ra_problem* prob, ra_plan_t* out) {
   ra_status s = validate(prob);
   if (s != RA_OK) return s;
   ra_plan_s* pl = new (std::nothrow) ra_plan_s();
-  if (pl == nullptr) return fail(RA_ERR_INVALID_ARG, "out of host memory");
+  if (pl == nullptr) return fail(RA_ERR_UNSUPPORTED, "out of host memory");
   pl->prob = *prob;
   if (pl->prob.scale == 0.f) pl->prob.scale = 1.0f / std::sqrt((float)prob->head_dim);
   pl->s_n = prob->seq / prob->n_shards;
@@ -510,14 +549,18 @@ ra_status ra_plan_destroy(ra_plan_t plan) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != plan->device) cudaSetDevice(plan->device);
-    // Kernels queued earlier on any stream may still read the work tables or the
-    // status word: let them finish before the memory goes back.
-    cudaDeviceSynchronize();
-    cudaFree(plan->d_items);
-    cudaFree(plan->d_step_items);
-    cudaFree(plan->d_bwd_items);
-    cudaFree(plan->d_gather_items);
-    cudaFree(plan->d_status);
+    // Kernels of this plan queued earlier may still read its work tables or its
+    // status word: the frees are queued behind them (and only them), in stream
+    // order, and the host does not wait.
+    if (plan->mem_stream != nullptr) {
+      for (const ra_plan_s::StreamMark& m : plan->marks) cudaStreamWaitEvent(plan->mem_stream, m.done, 0);
+      void* mem[] = {plan->d_items, plan->d_step_items, plan->d_bwd_items, plan->d_gather_items, plan->d_status};
+      for (void* p : mem)
+        if (p != nullptr) cudaFreeAsync(p, plan->mem_stream);
+      cudaStreamDestroy(plan->mem_stream);  // released once its queued frees have run
+    }
+    for (const ra_plan_s::StreamMark& m : plan->marks) cudaEventDestroy(m.done);
+    cudaGetLastError();
     if (plan->ev_entry) cudaEventDestroy(plan->ev_entry);
     if (plan->ev_rot) cudaEventDestroy(plan->ev_rot);
     if (plan->ev_step) cudaEventDestroy(plan->ev_step);
@@ -553,6 +596,7 @@ ra_status ra_fwd(ra_plan_t plan, const void* q, const void* k, const void* v, vo
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
   ra_status s = check_device(plan);
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 7, static_cast<cudaStream_t>(stream));
   if (s != RA_OK) return s;
   ra::FwdParams prm = fwd_params(plan);
   prm.items = plan->d_items;
@@ -574,6 +618,8 @@ ra_status ra_merge_partials(int32_t n_parts, int64_t rows, int32_t d, const floa
   const void* ptrs[] = {o_parts, lse_parts, o, lse};
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
+  const ra_status s = ra::check_on_current_device(ptrs, 4, static_cast<cudaStream_t>(stream));
+  if (s != RA_OK) return s;
   cudaError_t e = ra::launch_merge(n_parts, rows, d, o_parts, lse_parts, o, o_dtype, lse,
                                    static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(e));
@@ -593,6 +639,9 @@ ra_status ra_layout_perm(int32_t layout, int64_t seq, int32_t n_shards, int32_t 
   const char* a = static_cast<const char*>(src);
   const char* b = static_cast<const char*>(dst);
   if (a < b + bytes && b < a + bytes) return fail(RA_ERR_INVALID_ARG, "src and dst overlap");
+  const void* ptrs[] = {src, dst};
+  s = ra::check_on_current_device(ptrs, 2, static_cast<cudaStream_t>(stream));
+  if (s != RA_OK) return s;
   cudaError_t e = ra::launch_layout_perm(layout, seq, n_shards, inverse ? 1 : 0, rows_outer, row_bytes,
                                          src, dst, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "layout permute launch failed: %s", cudaGetErrorString(e));
@@ -621,6 +670,7 @@ ra_status ra_fwd_step(ra_plan_t plan, int32_t step, const void* q, const void* k
   for (const void* p : ptrs)
     if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
   ra_status s = check_device(plan);
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 5, static_cast<cudaStream_t>(stream));
   if (s != RA_OK) return s;
   ra::FwdParams prm = fwd_params(plan);
   prm.step_lo = (int16_t)step;
@@ -645,6 +695,8 @@ ra_status ra_ring_rotate(ra_plan_t plan, const void* k_src, const void* v_src, v
   if (overlap(k_src, k_dst, bytes) || overlap(v_src, v_dst, bytes) || overlap(k_dst, v_dst, bytes))
     return fail(RA_ERR_INVALID_ARG, "a destination overlaps its source or the other destination");
   ra_status s = check_device(plan);
+  const void* ptrs[] = {k_src, v_src, k_dst, v_dst};
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 4, static_cast<cudaStream_t>(stream));
   if (s != RA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = rotate_one(plan, k_src, k_dst, st);
@@ -670,6 +722,8 @@ ra_status ra_ring_fwd(ra_plan_t plan, const void* q, const void* k, const void* 
                 overlap(k_buf, v, kv_bytes) || overlap(v_buf, k, kv_bytes) || overlap(v_buf, v, kv_bytes)))
     return fail(RA_ERR_INVALID_ARG, "receive buffers overlap each other or K/V");
   ra_status s = check_device(plan);
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 9, static_cast<cudaStream_t>(stream));
+  if (s == RA_OK) s = ra::check_on_current_device(nullptr, 0, static_cast<cudaStream_t>(comm_stream));
   if (s != RA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaStream_t cs = static_cast<cudaStream_t>(comm_stream);
@@ -721,6 +775,7 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
     if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
   }
   ra_status s = check_device(plan);
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 10, static_cast<cudaStream_t>(stream));
   if (s != RA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t n64 = (plan->s_n + 63) / 64;
@@ -754,7 +809,8 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
     e = ra::launch_bwd_f32(prm, static_cast<const float*>(q), static_cast<const float*>(k),
                            static_cast<const float*>(v), static_cast<const float*>(dout), st);
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "f32 backward launch failed: %s", cudaGetErrorString(e));
-    return ok();
+    s = mark_use(plan, st);
+    return s != RA_OK ? s : ok();
   }
   const int sms = plan->sm_count > 0 ? plan->sm_count : 148;
   for (int pass = 0; pass < 2; ++pass) {
@@ -775,7 +831,8 @@ ra_status ra_bwd(ra_plan_t plan, const void* q, const void* k, const void* v, co
     }
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, "%s: %s", why, cudaGetErrorString(e));
   }
-  return ok();
+  s = mark_use(plan, st);
+  return s != RA_OK ? s : ok();
 }
 
 ra_status ra_allgather_kv(ra_plan_t plan, const void* k, const void* v, void* k_all, void* v_all, void* stream) {
@@ -790,6 +847,7 @@ ra_status ra_allgather_kv(ra_plan_t plan, const void* k, const void* v, void* k_
   if (overlap(k, k_all, bytes) || overlap(v, v_all, bytes) || overlap(k_all, v_all, bytes))
     return fail(RA_ERR_INVALID_ARG, "a destination overlaps its source or the other destination");
   ra_status s = check_device(plan);
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 4, static_cast<cudaStream_t>(stream));
   if (s != RA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int row_bytes = pb.head_dim * (int)elem_bytes(pb);
@@ -810,6 +868,7 @@ ra_status ra_fwd_gathered(ra_plan_t plan, const void* q, const void* k_all, cons
   for (const void* p : ptrs)
     if (p != nullptr && !aligned16(p)) return fail(RA_ERR_INVALID_ARG, "pointer %p is not 16-byte aligned", p);
   ra_status s = check_device(plan);
+  if (s == RA_OK) s = ra::check_on_current_device(ptrs, 5, static_cast<cudaStream_t>(stream));
   if (s != RA_OK) return s;
   ra::FwdParams prm = fwd_params(plan);
   prm.gathered = 1;
@@ -838,6 +897,9 @@ ra_status ra_ulysses_a2a(int32_t direction, int32_t layout, int64_t seq, int32_t
   if (!aligned16(src) || !aligned16(dst)) return fail(RA_ERR_INVALID_ARG, "src/dst must be 16-byte aligned");
   if (overlap(src, dst, (size_t)(batch * heads * seq) * row_bytes))
     return fail(RA_ERR_INVALID_ARG, "src and dst overlap");
+  const void* ptrs[] = {src, dst};
+  s = ra::check_on_current_device(ptrs, 2, static_cast<cudaStream_t>(stream));
+  if (s != RA_OK) return s;
   cudaError_t e = ra::launch_ulysses_a2a(direction, layout, n_shards, (int)batch, heads, seq, row_bytes, src, dst,
                                          static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "exchange launch failed: %s", cudaGetErrorString(e));

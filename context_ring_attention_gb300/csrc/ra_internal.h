@@ -4,6 +4,7 @@
 // that the host planner and every kernel use one definition of each.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -77,6 +78,52 @@ struct alignas(16) WorkItem {
   int32_t cost;   // key tiles visited (longest-first ordering key)
   int32_t pad;
 };
+
+// Work items of a bf16 forward per query shard: query tiles are paired per item,
+// two heads of a GQA group at the same rows when Hq/Hkv is even, else two
+// consecutive row tiles of one head.
+inline int64_t fwd_items_per_shard(const ra_problem& pb, int64_t s_n) {
+  const int64_t n_qt = (s_n + kTileRows - 1) / kTileRows;
+  return ((pb.heads_q / pb.heads_kv) % 2 == 0) ? n_qt * pb.batch * (pb.heads_q / 2)
+                                                : ((n_qt + 1) / 2) * pb.batch * pb.heads_q;
+}
+
+// The forward's work list in creation order: emit(item) for every item, each
+// costed by the key tiles it visits over the N ring steps.  The planner and the
+// plan-free entry point both build their lists here, so that both hand the
+// kernel the same items in the same schedule order.
+template <class Emit>
+void for_each_fwd_item(const ra_problem& pb, int64_t s_n, Emit&& emit) {
+  const int N = pb.n_shards;
+  const int n_qt = (int)((s_n + kTileRows - 1) / kTileRows);
+  const bool head_pairs = ((pb.heads_q / pb.heads_kv) % 2) == 0;
+  for (int p = 0; p < N; ++p)
+    for (int qt = 0; qt < n_qt; qt += head_pairs ? 1 : 2)
+      for (int64_t b = 0; b < pb.batch; ++b)
+        for (int h = 0; h < pb.heads_q; h += head_pairs ? 2 : 1) {
+          WorkItem w{};
+          w.bh0 = (int32_t)(b * pb.heads_q + h);
+          w.shard = p;
+          w.row0 = qt * kTileRows;
+          if (head_pairs) {
+            w.bh1 = w.bh0 + 1;
+            w.row1 = w.row0;
+          } else if (qt + 1 < n_qt) {
+            w.bh1 = w.bh0;
+            w.row1 = w.row0 + kTileRows;
+          } else {
+            w.bh1 = -1;
+            w.row1 = w.row0;
+          }
+          const int64_t top = (w.bh1 >= 0) ? w.row1 : w.row0;
+          const int64_t last = (top + kTileRows < s_n ? top + kTileRows : s_n) - 1;
+          w.maxq = (int32_t)pos_of(pb.layout, N, s_n, p, last);
+          int cost = 0;
+          for (int t = 0; t < N; ++t) cost += visit_tiles(pb.layout, N, s_n, pb.causal, (p - t + N) % N, w.maxq);
+          w.cost = cost;
+          emit(w);
+        }
+}
 
 // Schedule order of work items for the persistent grid, which hands items out
 // round-robin: longest first (so the grid ends evenly), but items whose cost lies
@@ -173,5 +220,51 @@ cudaError_t launch_ulysses_a2a(int dir, int layout, int n, int batch, int heads,
 
 // Sets the thread-local message returned by ra_last_error().
 void set_last_error(const char* msg);
+
+// RA_OK when every non-null pointer of ptrs[0..n) is device memory of the current
+// device (or managed memory) and the stream belongs to that device; otherwise
+// RA_ERR_INVALID_ARG (RA_ERR_NO_DEVICE without a device), with the message set.
+// The kernels run on the current device and read every buffer through it: a
+// buffer of another device would be read through a mapping it may not have.
+ra_status check_on_current_device(const void* const* ptrs, int n, cudaStream_t stream);
+
+// Device ordinals below this get per-device launch state (kernel attributes set
+// once per device, the plan-free entry point's scratch address).
+constexpr int kMaxDevices = 64;
+
+// Launch preparation of a warp-specialised tensor-core kernel, done once per
+// device (ready[] is the kernel's own flag array): the kernel must have been
+// built with at least regs_needed registers per CTA (setmaxnreg.inc waits for
+// registers that exist only in the launch's allocation), and its dynamic
+// shared-memory limit is raised to smem_bytes.
+template <class Kernel>
+cudaError_t prepare_once(Kernel kernel, std::atomic<int>* ready, uint32_t threads, uint32_t regs_needed,
+                         int smem_bytes, const char** why) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    *why = "cudaGetDevice failed";
+    return e;
+  }
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && ready[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kernel);
+  if (e != cudaSuccess) {
+    *why = "cudaFuncGetAttributes failed";
+    return e;
+  }
+  if ((uint32_t)attr.numRegs * threads < regs_needed) {
+    *why = "kernel was built with fewer launch registers than its warpgroup split needs";
+    return cudaErrorInvalidConfiguration;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) {
+    *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
+  }
+  if (cached) ready[dev].store(1, std::memory_order_release);
+  return cudaSuccess;
+}
 
 }  // namespace ra

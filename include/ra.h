@@ -43,6 +43,10 @@
  *
  * Errors: every call returns an ra_status; on failure ra_last_error() returns a
  * thread-local message.  Arguments are checked before anything is launched.
+ * Every device buffer must be memory of the CURRENT device (or managed memory)
+ * and every stream must belong to it: the kernels run on the current device, so
+ * a buffer of another device or a host pointer is rejected with
+ * RA_ERR_INVALID_ARG before any launch (RA_ERR_NO_DEVICE when no device exists).
  * Uneven shards are rejected, never padded (Module 23, "Common Pitfalls":
  * reject uneven shards rather than silently bias the result).
  */
@@ -100,8 +104,10 @@ typedef struct ra_plan_s* ra_plan_t;
  * passes (ra_bwd), each in longest-first order with key/value heads grouped.  It
  * also picks each kernel's schedule: synchronised rounds when one key/value head's
  * K and V exceed 32 MiB, otherwise items handed out as CTAs free up.  When a CUDA
- * device is current, it uploads the work tables, allocates the plan's device status
- * word and creates the three events ra_ring_fwd orders its streams with.  Without a
+ * device is current, it uploads the work tables and allocates the plan's device
+ * status word (stream-ordered, on a stream of the plan's own; the call returns once
+ * they are in place), and creates the three events ra_ring_fwd orders its streams
+ * with.  Without a
  * device the plan is host-only: tile counts work, the compute calls return
  * RA_ERR_NO_DEVICE.
  * *out receives the plan; release it with ra_plan_destroy.
@@ -113,9 +119,14 @@ typedef struct ra_plan_s* ra_plan_t;
  */
 ra_status ra_plan(const ra_problem* prob, ra_plan_t* out);
 
-/* Release a plan and its device memory.  NULL is accepted.  It first waits for the
- * plan's device to finish the work queued so far (which may still read the plan's
- * tables), so it is synchronous; it does not clear a pending CUDA error. */
+/* Release a plan and its device memory.  NULL is accepted.  It does not wait:
+ * kernels queued with this plan may still read its tables, so the plan records
+ * an event on every stream it launched on (after its latest launch there), and
+ * the frees of its device memory are queued in stream order behind those events
+ * only (cudaFreeAsync on the plan's own stream; the plan allocated its tables
+ * with cudaMallocAsync).  Other streams' work and other plans' kernels are not
+ * waited for.  Do not use the plan after this call.  It does not clear a pending
+ * CUDA error. */
 ra_status ra_plan_destroy(ra_plan_t plan);
 
 /*
@@ -370,7 +381,7 @@ ra_status ra_sync_status(ra_plan_t plan, void* stream);
  *     start of each call.  Calls whose kernels overlap on the GPU race on the
  *     array and must not be issued; calls from several host threads are
  *     serialised on the host.  Device-side wait timeouts are recorded in the
- *     array's status word but not reported (use a plan and ra_sync_status for that).
+ *     array's status word, which ra_fwd_static_status reports.
  * prob: the problem (dtype RA_DTYPE_BF16, head_dim 128).  q, k, v, o, lse: as for
  * ra_fwd in fused mode (lse may be NULL), device pointers, 16-byte aligned.
  * Asynchronous on stream.
@@ -379,6 +390,18 @@ ra_status ra_sync_status(ra_plan_t plan, void* stream);
  */
 ra_status ra_fwd_static(const ra_problem* prob, const void* q, const void* k, const void* v,
                         void* o, float* lse, void* stream);
+
+/*
+ * ra_fwd_static_status -- the device-wait status of the latest ra_fwd_static
+ * call on the current device.  Like ra_fwd_static, no counterpart on the pages.
+ * Synchronizes `stream` (the stream that call ran on), then reads and clears the
+ * status word in the static array: RA_ERR_TIMEOUT if that call's kernel gave up
+ * on a device-side wait (its O/LSE are then incomplete), RA_OK otherwise or when
+ * ra_fwd_static has not run on this device.  It allocates nothing.  The next
+ * ra_fwd_static call clears the word, so read it before issuing another.
+ * Errors: RA_ERR_TIMEOUT, RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ */
+ra_status ra_fwd_static_status(void* stream);
 
 /*
  * ra_wait_selftest -- check the failure-detection path of the tensor-core kernels.

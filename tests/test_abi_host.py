@@ -219,7 +219,8 @@ def test_binding_buffer_check():
     # the binding's check on caller buffers (shape, dtype, contiguity, device)
     torch = pytest.importorskip("torch")
     cpu = torch.device("cpu")
-    ra._need("t", torch.empty((2, 3, 4)), (2, 3, 4), torch.float32, cpu)
+    with pytest.raises(ValueError):   # right shape, dtype and layout, but not on a CUDA device
+        ra._need("t", torch.empty((2, 3, 4)), (2, 3, 4), torch.float32, cpu)
     for bad in (torch.empty((2, 3, 5)), torch.empty((2, 3, 4), dtype=torch.bfloat16),
                 torch.empty((2, 4, 3)).transpose(1, 2), "not a tensor"):
         with pytest.raises(ValueError):
