@@ -65,6 +65,19 @@ def job_rate(world, flops_per_rank, ms):
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
+# Dense bf16 tensor-core rate of one SM per clock: a 128 x 256 x 16 MMA (1,048,576
+# FLOP) issues every 128 cycles.  152 SMs at 2070 MHz give 2577 TFLOP/s; a stand-alone
+# MMA issue loop measured 2430 TFLOP/s (0.94 of it) at that clock.
+TC_FLOP_PER_CLK_SM = 8192
+
+
+def clock_peak(sms, sm_mhz):
+    """The tensor pipe's issue-rate peak (TFLOP/s) at the SM clock the kernel ran at."""
+    if not sm_mhz:
+        return None
+    return sms * TC_FLOP_PER_CLK_SM * float(sm_mhz) * 1e6 / 1e12
+
+
 # A (batch, key/value head) unit of the end-to-end pipeline needs this many FLOPs
 # (about 0.1 s of forward) before a step is split into such units.
 E2E_UNIT_FLOPS = 2e14
@@ -131,6 +144,76 @@ class ClockSampler:
 
 # ------------------------------------------------------------- CPU oracle --
 
+def blas_threads():
+    """Threads of the BLAS numpy calls (None when it cannot be asked)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            libs = sorted({ln.split()[-1] for ln in f if "blas" in ln.lower() and ".so" in ln})
+    except OSError:
+        return None
+    for lib in libs:
+        try:
+            h = ctypes.CDLL(lib)
+        except OSError:
+            continue
+        for name in ("openblas_get_num_threads", "scipy_openblas_get_num_threads64_",
+                     "openblas_get_num_threads64_", "scipy_openblas_get_num_threads"):
+            fn = getattr(h, name, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
+
+
+def ring_sim_timings():
+    """The ring simulation oracle (the Q&A page's N-round loop) timed on the two small
+    workloads: the toy ring in full, and one (batch, head) of the 4k non-causal ring
+    (extrapolated to its 64 heads)."""
+    import oracle
+    from context_ring_attention_gb300 import workloads
+    out = {}
+    toy = workloads.WORKLOADS["toy_ring_4x3_d8"]
+    q, k, v = (a.reshape(1, 1, 12, 8) for a in workloads.toy_inputs())
+    reps = 200
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.ring_sim(q, k, v, toy.n_shards)
+    dt = (time.perf_counter() - t0) / reps
+    out[toy.name] = {"seconds": dt, "TFLOP/s": toy.flops() / dt / 1e12, "sample": "whole problem"}
+    wl = workloads.WORKLOADS["noncausal_4k_n8"]
+    rng = np.random.default_rng(12)
+    q, k, v = (rng.standard_normal((1, 1, wl.seq, wl.head_dim)) for _ in range(3))
+    t0 = time.perf_counter()
+    oracle.ring_sim(q, k, v, wl.n_shards)
+    dt = time.perf_counter() - t0
+    per_head = wl.flops() / (wl.batch * wl.heads_q)
+    out[wl.name] = {"seconds": dt, "TFLOP/s": per_head / dt / 1e12,
+                    "sample": f"one (batch, head) of {wl.batch * wl.heads_q}, N(0,1) float64",
+                    "extrapolated_full_s": dt * wl.batch * wl.heads_q}
+    return out
+
+
+def cpu_baseline_record(wl, rows, seed=11, with_ring_sim=True):
+    """The cpu_baseline object: the oracle's rate on a bounded sample, the threads it
+    ran on, and the whole workload's time extrapolated from that rate."""
+    v_cpu, dt, _, desc = cpu_oracle_sample(wl, rows=rows, seed=seed)
+    rec = {"value": v_cpu, "unit": "TFLOP/s", "cores": os.cpu_count(), "blas_threads": blas_threads(),
+           "kind": "oracle", "sample": desc, "seconds": dt,
+           "extrapolated_full_s": wl.flops() / (v_cpu * 1e12),
+           "extrapolated_note": "whole workload at the sample's rate (extrapolated, not run)"}
+    if with_ring_sim:
+        rec["ring_sim"] = ring_sim_timings()
+    return rec
+
+
 def cpu_oracle_sample(wl, rows=192, seed=11):
     """Time the float64 oracle on `rows` causal query rows of one key/value head.
 
@@ -169,12 +252,15 @@ def run_reference(args, wl):
             tf.append(v)
     value = statistics.median(tf)
     cores = os.cpu_count()
+    full_s = wl.flops() / (value * 1e12)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_of(wl),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "blas_threads": blas_threads(),
+                         "kind": "oracle", "sample": desc, "extrapolated_full_s": full_s,
+                         "extrapolated_note": "whole workload at the sample's rate (extrapolated, not run)"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -447,6 +533,9 @@ def run_ours(args, wl):
     fwd_mean = statistics.mean(fwd_ms)
     achieved = flops / (fwd_mean * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    clocks = clk.summary()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    at_clock = clock_peak(sms, clocks.get("sm_mhz"))
     traffic = measured_traffic(wl.name)
     full, part, skip = ra.ra_plan_tile_counts(plan)
     line = {
@@ -457,10 +546,14 @@ def run_ours(args, wl):
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{src} bf16_tflops_sustained",
                      "frac_of_burst": achieved / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                     "frac_at_clock": achieved / at_clock if at_clock else None,
+                     "peak_at_clock": at_clock,
+                     "peak_at_clock_note": (f"{sms} SMs x {TC_FLOP_PER_CLK_SM} dense bf16 FLOP per SM clock x the "
+                                            "median SM clock sampled during the timed steps"),
                      "fwd_ms_mean": fwd_mean},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "tile_counts": {"full": full.tolist(), "partial": part.tolist(), "skip": skip.tolist(),
                         "granularity": "128x128 per (batch, query head)"},
         "algorithmic_flops_per_step": flops,
@@ -493,9 +586,7 @@ def run_ours(args, wl):
         for kv in kernels.values():
             kv["frac_of_hbm"] = kv["GB/s"] / hbm
     if world == 1 and not args.no_cpu_baseline:
-        v_cpu, dt, _, desc = cpu_oracle_sample(wl, rows=args.ref_rows)
-        line["cpu_baseline"] = {"value": v_cpu, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": desc, "seconds": dt}
+        line["cpu_baseline"] = cpu_baseline_record(wl, args.ref_rows)
     print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
