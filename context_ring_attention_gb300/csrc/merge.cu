@@ -2,8 +2,11 @@
 // online-softmax fold, Module 23, "The Math: One Block at a Time"):
 //   LSE = ln sum_t e^(LSE_t),   O = sum_t e^(LSE_t - LSE) O_t.
 // HBM-bound: one warp per row, 16-byte loads along d.  For d = 128 (the attention
-// case) a lane owns 4 columns; the part weights are computed once per row by the
-// lanes t < n_parts and broadcast, and eight parts' loads are in flight at once.
+// case) a lane owns 4 columns and the part weights are computed once per row by the
+// lanes t < n_parts and broadcast.  Up to 8 parts (a ring of up to 8 devices), a
+// warp takes two rows at a time and issues every load of both rows -- 16 blocks of
+// 512 bytes and the LSEs -- before any arithmetic, so that enough bytes are in
+// flight per SM to cover the HBM latency.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -79,7 +82,67 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// d = 128: lane owns columns 4*lane .. 4*lane + 3 of every part.
+__device__ __forceinline__ void store_row(void* o, int64_t row, int lane, float4 a, bool bf16_out) {
+  if (bf16_out) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(o)[row * 32 + lane] = pk;
+  } else {
+    reinterpret_cast<float4*>(o)[row * 32 + lane] = a;
+  }
+}
+
+// d = 128 and n_parts <= kFewParts: kRowsPerWarp rows per warp at a time, all loads first.
+constexpr int kFewParts = 8;
+constexpr int kRowsPerWarp = 2;
+template <bool kBf16Out>
+__global__ void __launch_bounds__(kWarps * 32)
+    merge_d128_few_kernel(int n_parts, int64_t rows, const float4* __restrict__ o_parts,
+                          const float* __restrict__ lse_parts, void* __restrict__ o, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t first = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * kRowsPerWarp;
+  const int64_t stride = (int64_t)gridDim.x * kWarps * kRowsPerWarp;
+  for (int64_t r0 = first; r0 < rows; r0 += stride) {
+    float lt[kRowsPerWarp];
+    float4 x[kRowsPerWarp][kFewParts];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int64_t row = r0 + r;
+      const bool in = row < rows;
+      lt[r] = (in && lane < n_parts) ? lse_parts[(int64_t)lane * rows + row] : -INFINITY;
+#pragma unroll
+      for (int b = 0; b < kFewParts; ++b)
+        x[r][b] = (in && b < n_parts) ? o_parts[((int64_t)b * rows + row) * 32 + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int64_t row = r0 + r;
+      if (row >= rows) break;  // warp-uniform
+      const float top = warp_max(lt[r]);
+      const float e = (top != -INFINITY && lt[r] != -INFINITY) ? expf(lt[r] - top) : 0.f;
+      const float z = warp_sum(e);
+      const float big = (top != -INFINITY) ? top + logf(z) : -INFINITY;
+      const float w_lane = (big != -INFINITY && lt[r] != -INFINITY) ? expf(lt[r] - big) : 0.f;
+      if (lane == 0 && lse != nullptr) lse[row] = big;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int b = 0; b < kFewParts; ++b) {
+        const float w = __shfl_sync(0xffffffffu, w_lane, b);
+        if (b < n_parts && w != 0.f) {  // a part with LSE = -inf adds nothing (its O may be anything)
+          a.x = fmaf(w, x[r][b].x, a.x);
+          a.y = fmaf(w, x[r][b].y, a.y);
+          a.z = fmaf(w, x[r][b].z, a.z);
+          a.w = fmaf(w, x[r][b].w, a.w);
+        }
+      }
+      store_row(o, row, lane, a, kBf16Out);
+    }
+  }
+}
+
+// d = 128, more parts: lane owns columns 4*lane .. 4*lane + 3 of every part.
 template <bool kBf16Out>
 __global__ void __launch_bounds__(kWarps * 32)
     merge_d128_kernel(int n_parts, int64_t rows, const float4* __restrict__ o_parts,
@@ -113,15 +176,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         }
       }
     }
-    if (kBf16Out) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
-      uint2 pk;
-      pk.x = *reinterpret_cast<uint32_t*>(&lo);
-      pk.y = *reinterpret_cast<uint32_t*>(&hi);
-      reinterpret_cast<uint2*>(o)[row * 32 + lane] = pk;
-    } else {
-      reinterpret_cast<float4*>(o)[row * 32 + lane] = a;
-    }
+    store_row(o, row, lane, a, kBf16Out);
   }
 }
 
@@ -135,6 +190,17 @@ cudaError_t launch_merge(int n_parts, int64_t rows, int d, const float* o_parts,
   int64_t blocks = (rows + kWarps - 1) / kWarps;
   const int64_t cap = (int64_t)sms * 16;
   if (blocks > cap) blocks = cap;
+  if (d == 128 && n_parts <= kFewParts) {
+    int64_t few_blocks = (rows + kWarps * kRowsPerWarp - 1) / (kWarps * kRowsPerWarp);
+    if (few_blocks > cap) few_blocks = cap;
+    if (o_dtype == RA_DTYPE_BF16)
+      merge_d128_few_kernel<true><<<(unsigned)few_blocks, kWarps * 32, 0, stream>>>(
+          n_parts, rows, reinterpret_cast<const float4*>(o_parts), lse_parts, o, lse);
+    else
+      merge_d128_few_kernel<false><<<(unsigned)few_blocks, kWarps * 32, 0, stream>>>(
+          n_parts, rows, reinterpret_cast<const float4*>(o_parts), lse_parts, o, lse);
+    return cudaGetLastError();
+  }
   if (d == 128 && n_parts <= 32) {
     if (o_dtype == RA_DTYPE_BF16)
       merge_d128_kernel<true><<<(unsigned)blocks, kWarps * 32, 0, stream>>>(

@@ -46,7 +46,8 @@ def test_layout_perm_bitexact(layout, seq, n):
 
 # ------------------------------------------------------------------ merge --
 
-@pytest.mark.parametrize("n_parts,rows,d", [(8, 1000, 128), (3, 77, 8), (32, 300, 128), (1, 5, 13), (1, 64, 128), (40, 100, 128)])
+@pytest.mark.parametrize("n_parts,rows,d", [(8, 1000, 128), (5, 1001, 128), (3, 77, 8), (32, 300, 128), (9, 33, 128),
+                                             (1, 5, 13), (1, 64, 128), (40, 100, 128)])
 @pytest.mark.parametrize("out", ["f32", "bf16"])
 def test_merge_matches_oracle(n_parts, rows, d, out):
     g = torch.Generator(device="cuda").manual_seed(n_parts * 1000 + rows)
