@@ -17,7 +17,8 @@
 //   issues each instruction: a single divergent lane issues MMAs too slowly to
 //   keep the tensor pipe fed while the softmax warps share its scheduler.
 //   warps 4-7  softmax for query tile 0, warps 8-11 for query tile 1: one thread
-//              per row reads its 128 scores from TMEM in one round trip, updates
+//              per row reads its 128 scores from TMEM in one round trip (a reducing
+//              load, which also returns the row's largest score), updates
 //              m and l, writes P (bf16) back into the upper half of its S columns,
 //              rescales O in TMEM when m moves, and writes O / l and the LSE at the
 //              end of a segment.
@@ -496,42 +497,52 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
         }
         continue;
       }
-      const int64_t kv_rows = kGathered ? P.seq : P.s_n;  // rows of the key block met
-      const int64_t J = !P.causal ? kv_rows - 1
-                                  : (kGathered ? my_pos : last_le(P.layout, N, P.s_n, r, my_pos));
+      // How many leading keys of the block met the row may see: all of its rows, or
+      // (causal) those up to its last key at or before the row's position.  Rows and
+      // positions fit in 32 bits (S is at most 2^31 - 1).
+      const int kv_rows = (int)(kGathered ? P.seq : P.s_n);
+      const int seen = !P.causal ? kv_rows
+                                 : 1 + (int)(kGathered ? my_pos : last_le(P.layout, N, P.s_n, r, my_pos));
+      const int keys = seen < kv_rows ? seen : kv_rows;
       for (int kt = 0; kt < nt; ++kt) {
         const bool first = partials ? (kt == 0) : !open;
         const bool last = partials ? (kt == nt - 1) : (t == last_t && kt == nt - 1);
         open = true;
-        const int64_t j0 = (int64_t)kt * kTileRows;
-        int64_t lim = J - j0 + 1;
-        const int64_t cap = (kv_rows - j0 < kTileRows) ? kv_rows - j0 : kTileRows;
-        lim = lim < 0 ? 0 : (lim > cap ? cap : lim);
-        const int limit = (int)lim;
+        int limit = keys - kt * kTileRows;  // keys of this tile the row sees
+        limit = limit < 0 ? 0 : (limit > kTileRows ? kTileRows : limit);
 
         bool ok = wait_bar(c, c.bar(kSFull + g), sj & 1u, kStatusTimeoutSoftmax);
         ++sj;
         if (!__all_sync(0xffffffffu, ok)) return;
         ptx::tc_fence_after();
 
-        // The whole 128-column score row in registers (one TMEM round trip).
+        // The whole 128-column score row in registers (one TMEM round trip); the
+        // reducing load also returns the largest score of each 32 columns.
         uint32_t raw[128];
-        ptx::tmem_ld128(tS, raw);
+        float mx4[4];
+        ptx::tmem_ld128_max(tS, raw, mx4);
         float* s = reinterpret_cast<float*>(raw);
-        if (limit < kTileRows) {  // causal diagonal / ragged tail: masked keys score -inf
+        float mx;
+        if (limit < kTileRows) {
+          // Causal diagonal / ragged tail: masked keys score -inf and the row max is
+          // taken over the rest, with eight independent partial maxima: columns
+          // a, a+8, ..., a+120 go to partial a.
 #pragma unroll
           for (int e = 0; e < 128; ++e) s[e] = (e < limit) ? s[e] : -INFINITY;
+          float mx8[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx8[a] = ptx::max3(s[a], s[a + 8], s[a + 16]);
+#pragma unroll
+          for (int e = 24; e + 16 <= 120; e += 16)
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx8[a] = ptx::max3(mx8[a], s[e + a], s[e + 8 + a]);
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mx8[a] = fmaxf(mx8[a], s[120 + a]);
+          mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
+                     fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        } else {
+          mx = fmaxf(ptx::max3(mx4[0], mx4[1], mx4[2]), mx4[3]);
         }
-        // Row max with independent partial maxima (no long dependency chain).
-        float mx8[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mx8[a] = ptx::max3(s[a], s[a + 8], s[a + 16]);
-#pragma unroll
-        for (int e = 24; e + 16 <= 128; e += 16)
-#pragma unroll
-          for (int a = 0; a < 8; ++a) mx8[a] = ptx::max3(mx8[a], s[e + a], s[e + 8 + a]);
-        const float mx = fmaxf(ptx::max3(mx8[0], mx8[1], mx8[2]),
-                               fmaxf(ptx::max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float mt = mx * sl2;  // in log2 units; -inf stays -inf
         float m_new = m;
         bool resc = false;
@@ -567,7 +578,9 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
         // The PV MMA weighs each key by its bf16-rounded p while l sums the fp32 p.
         // Replace the tile's largest p by its rounded value in l as well: when one
         // key dominates a row, its rounding then cancels in o / l.
-        const float p_top = ptx::ex2_approx(fmaf(mx, sl2, -mref));
+        // (computed by the same packed multiply-add as the loop's p, so that it is
+        // bit for bit the p of the row's largest score)
+        const float p_top = ptx::ex2_approx(ptx::fma2(make_float2(mx, mx), sc2, neg).x);
         const float p_top_bf = __uint_as_float(ptx::pack_bf16x2(p_top, 0.f) << 16);
         const float top_fix = p_top_bf - p_top;
         if (!first && __any_sync(0xffffffffu, resc)) {

@@ -73,6 +73,31 @@ def test_bf16_large_logits(causal):
     _run(1, 1024, 4, 2, 4, "zigzag", causal, seed=10, q_scale=4.0, scale=0.3)
 
 
+@pytest.mark.parametrize("n", [1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_dominant_key_in_last_columns(n, causal):
+    # One key (position 124, column 124 of its 128-key tile) scores about 260 log2
+    # units above every other key for the queries at positions 120..127.  The row max
+    # must include the tile's last columns: a reference that missed that key would put
+    # 2^260 into float32 and turn those rows into inf / NaN.  Rows 124..126 see the key
+    # through a causal diagonal tile (limit 125..127), rows 127 and up through a full one.
+    B, S, H, d = 1, 256, 1, 128
+    q, k, v = workloads.small_inputs(B, S, H, H, d, seed=31, device="cuda", dtype="bf16")
+    q[0, 0, 120:128] = 0
+    q[0, 0, 120:128, 0] = 16.0
+    k[0, 0, 124] = 0
+    k[0, 0, 124, 0] = 128.0
+    plan = ra.ra_plan(B, S, H, H, d, n, "contiguous", causal, "bf16")
+    o, lse = ra.ra_fwd(plan, q, k, v)
+    ra.ra_sync_status(plan)
+    ow, lw = oracle.full_attention(to64(q), to64(k), to64(v), causal=causal)
+    assert np.isfinite(to64(o)).all() and np.isfinite(to64(lse)).all()
+    # where the key is visible its weight is 1: the row is V's row 124, the LSE its score
+    seen = slice(124, 128) if causal else slice(120, 128)
+    assert np.array_equal(to64(o)[0, 0, seen], np.broadcast_to(to64(v)[0, 0, 124], to64(o)[0, 0, seen].shape))
+    assert_bf16_close(to64(o), ow, to64(lse), lw, f"dominant key causal={causal} N={n}")
+
+
 @pytest.mark.parametrize("layout", oracle.LAYOUTS)
 @pytest.mark.parametrize("causal", [False, True])
 def test_bf16_partials_and_merge(layout, causal):
