@@ -36,8 +36,11 @@
  *
  * Ownership: the caller owns every device buffer passed in.  A plan owns its
  * host tables, its device work tables (whole forward, one per ring step, backward),
- * its device status word and three CUDA events; ra_fwd, ra_fwd_step, ra_ring_rotate,
- * ra_ring_fwd, ra_bwd, ra_merge_partials and ra_layout_perm allocate nothing and are
+ * its device status word, a stream for its own allocations and frees, three CUDA
+ * events for ra_ring_fwd, and one event per stream its kernels were launched on;
+ * ra_fwd, ra_fwd_step, ra_ring_rotate, ra_ring_fwd, ra_bwd, ra_merge_partials and
+ * ra_layout_perm allocate no device memory ("allocates nothing" below: the first
+ * launch of a plan on a stream it has not used creates that stream's event) and are
  * asynchronous on the given stream (a cudaStream_t passed as void*; NULL = legacy
  * default).
  *
