@@ -50,8 +50,8 @@ struct ra_plan_s {
   bool round_sync = false;  // forward kernel schedule (ra::use_round_sync)
   int sm_count = 0;
   // One event per stream the plan's kernels were queued on, recorded after the
-  // latest of them: ra_plan_destroy waits for exactly this work before it frees the
-  // device tables.  A slot whose event has completed is reused for a new stream.
+  // latest of them: ra_plan_destroy queues the frees of the device tables behind
+  // exactly this work.  A slot whose event has completed is reused for a new stream.
   struct StreamMark {
     cudaStream_t stream;
     cudaEvent_t done;
@@ -424,7 +424,7 @@ ra_status check_device(const ra_plan_s* plan) {
 }
 
 // Record, on `st`, that the plan's device tables are in use by the work queued there
-// so far (ra_plan_destroy waits for it).
+// so far (ra_plan_destroy queues its frees behind it).
 ra_status mark_use(ra_plan_s* plan, cudaStream_t st) {
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) cudaGetLastError();
