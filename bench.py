@@ -550,7 +550,8 @@ def run_ours(args, wl):
                      "peak_at_clock": at_clock,
                      "peak_at_clock_note": (f"{sms} SMs x {TC_FLOP_PER_CLK_SM} dense bf16 FLOP per SM clock x the "
                                             "median SM clock sampled during the timed steps"),
-                     "fwd_ms_mean": fwd_mean},
+                     "fwd_ms_mean": fwd_mean, "fwd_ms_median": statistics.median(fwd_ms),
+                     "fwd_ms_all": fwd_ms},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
