@@ -34,7 +34,7 @@ __all__ = [
 LAYOUTS = {"contiguous": 0, "striped": 1, "zigzag": 2}
 DTYPES = {"f32": 0, "bf16": 1}
 _STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
-           4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE"}
+           4: "RA_ERR_TIMEOUT", 5: "RA_ERR_NO_DEVICE", 6: "RA_ERR_BOUNDS"}
 EXPORTED = ("ra_plan", "ra_plan_destroy", "ra_plan_tile_counts", "ra_fwd", "ra_merge_partials",
             "ra_layout_perm", "ra_layout_index", "ra_sync_status", "ra_last_error", "ra_fwd_static",
             "ra_fwd_static_status", "ra_fwd_step", "ra_ring_rotate", "ra_ring_fwd", "ra_bwd", "ra_bwd_scratch_size",
@@ -59,7 +59,10 @@ class _Problem(ctypes.Structure):
 
 
 def library_path():
-    return os.path.join(_HERE, "libra.so")
+    """libra.so, or with RA_LIBRARY_VARIANT=debug in the environment libra_debug.so: the same
+    library with the kernels' bounds checks compiled in (built by build.build_all())."""
+    name = "libra_debug.so" if os.environ.get("RA_LIBRARY_VARIANT") == "debug" else "libra.so"
+    return os.path.join(_HERE, name)
 
 
 def load_library():
@@ -69,7 +72,7 @@ def load_library():
         return _LIB
     path = library_path()
     if not os.path.exists(path):
-        raise RuntimeError(f"{path} is not built; run context_ring_attention_gb300.build.build()")
+        raise RuntimeError(f"{path} is not built; run context_ring_attention_gb300.build.build_all()")
     lib = ctypes.CDLL(path)
     P, I32, I64, VP = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     sig = {

@@ -318,12 +318,16 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
     if (idx < 0) break;
+    RA_BOUNDS(c.status, idx < P.n_items, 20);
     const WorkItem it = P.items[idx];
+    RA_BOUNDS(c.status, it.shard >= 0 && it.shard < P.n_shards && it.row0 >= 0 && it.row0 < P.s_n, 21);
+    const int64_t rows_q = (int64_t)P.batch * P.heads_q * P.seq, rows_kv = (int64_t)P.batch * P.heads_kv * P.seq;
     if (kPass == 0) {
       if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kFixEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
       // The item's own tiles: rows bh0*S + shard*s_n + row0 of K and V.  (Pass 1's own
       // Q and dO rows go to tensor memory through the elementwise warps.)
       const int32_t yf = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
+      RA_BOUNDS(c.status, yf >= 0 && yf < rows_kv, 22);
       ptx::mbar_arrive_expect_tx_warp(c.bar(kFixFull), 2 * kFixBytes);
       ptx::tma_load_2d_warp(sbase + C::kOffFix, tx0, c.bar(kFixFull), 0, yf);
       ptx::tma_load_2d_warp(sbase + C::kOffFix + kFixHalf, tx0, c.bar(kFixFull), 64, yf);
@@ -347,6 +351,9 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
       const int64_t head_row = kPass == 0 ? ((int64_t)b * P.heads_q + h_base + w.g) * P.seq
                                           : ((int64_t)b * P.heads_kv + h_base) * P.seq;
       const int32_t y = (int32_t)(head_row + (int64_t)w.shard * P.s_n + (int64_t)w.it * kStreamRows);
+      RA_BOUNDS(c.status, w.shard >= 0 && w.shard < P.n_shards && w.it >= 0 && (int64_t)w.it * kStreamRows < P.s_n &&
+                              w.g >= 0 && w.g < (kPass == 0 ? P.group : 1), 23);
+      RA_BOUNDS(c.status, y >= 0 && y < (kPass == 0 ? rows_q : rows_kv), 24);
       const uint32_t s = s_it % C::kStages, phase = (s_it / C::kStages) & 1u;
       if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kStFull + C::kStages + (int)s), phase ^ 1u, kStatusTimeoutProducer))) {
         ok = false;
@@ -358,6 +365,11 @@ __device__ void run_producer(const BwdParams& P, const Ctl& c, uint32_t sbase, v
       ptx::tma_load_2d_warp_hint(dst + kStrHalf, ty0, c.bar(kStFull + (int)s), 64, y, keep);
       ptx::tma_load_2d_warp_hint(dst + kStrBytes, ty1, c.bar(kStFull + (int)s), 0, y, keep);
       ptx::tma_load_2d_warp_hint(dst + kStrBytes + kStrHalf, ty1, c.bar(kStFull + (int)s), 64, y, keep);
+      RA_BOUNDS(c.status,
+                kPass != 0 || bwd_scalar_index((int64_t)b * P.heads_q + h_base + w.g, w.shard, (int64_t)w.it * kStreamRows,
+                                               P.n_shards, P.n64) + 128 <=
+                                  (int64_t)P.batch * P.heads_q * P.n_shards * P.n64 * 128,
+                25);
       if (kPass == 0)  // the tile's 64 lse2 and 64 D values (one 512-byte block)
         ptx::bulk_load_warp(dst + 2 * kStrBytes,
                             P.lse2d + bwd_scalar_index((int64_t)b * P.heads_q + h_base + w.g, w.shard,
@@ -413,6 +425,8 @@ __device__ void run_mma(const BwdParams& P, const Ctl& c, uint32_t sbase, volati
   constexpr uint32_t NB = (uint32_t)C::kBufs;
   const int lane = threadIdx.x & 31;
   const uint32_t fix_lo = ptx::desc_lo(sbase + C::kOffFix, 16);
+  // two 128-column buffers, then the accumulators (and pass 1's Q, dO) up to column 512
+  RA_BOUNDS(c.status, tmem == 0u && col_buf(C::kBufs) <= col_acc0<kPass>() && kColDO + 64u <= kTmemCols, 26);
   uint32_t s_it = 0;  // streamed tiles so far (global tile index J of this CTA)
   auto str_lo = [&](uint32_t J, uint32_t lbo) {
     return ptx::desc_lo(sbase + C::kOffStage + (J % C::kStages) * C::kStageBytes, lbo);
@@ -524,10 +538,14 @@ __device__ void run_elementwise(const BwdParams& P, const Ctl& c, const uint8_t*
     const bool valid = i_own < P.s_n;
     const int64_t my_pos = pos_of(P.layout, N, P.s_n, it.shard, valid ? i_own : P.s_n - 1);
     const int64_t out_row = (int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + i_own;
+    RA_BOUNDS(c.status,
+              !valid || (out_row >= 0 && out_row < (int64_t)P.batch * (kPass == 0 ? P.heads_kv : P.heads_q) * P.seq), 27);
+    RA_BOUNDS(c.status, wq >= 0 && wq < 4 && (lane_off >> 16) + 32u <= 128u, 28);
     float2 own_l = make_float2(0.f, 0.f), own_d = make_float2(0.f, 0.f);  // pass 1: this row's lse2, D
     if (kPass == 1) {
       if (valid) {
         const int64_t li = bwd_scalar_index(it.bh0, it.shard, i_own, N, P.n64);
+        RA_BOUNDS(c.status, li >= 0 && li + 64 < (int64_t)P.batch * P.heads_q * N * P.n64 * 128, 29);
         own_l = make_float2(P.lse2d[li], P.lse2d[li]);
         own_d = make_float2(P.lse2d[li + 64], P.lse2d[li + 64]);
       }

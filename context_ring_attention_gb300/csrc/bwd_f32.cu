@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
   __syncwarp();
   const int64_t li = bwd_scalar_index(bh, p, i, N, P.n64);
+  RA_BOUNDS(P.status, li >= 0 && li + 64 < (int64_t)P.batch * P.heads_q * N * P.n64 * 128, 41);
   const float2 ld = make_float2(P.lse2d[li], P.lse2d[li + 64]);
   float acc[kMaxD / 32];
 #pragma unroll
@@ -118,6 +119,8 @@ __global__ void __launch_bounds__(kWarps * 32)
         if (i < P.s_n) {
           const int64_t row = qrow0 + i;
           const int64_t li = bwd_scalar_index((int64_t)b * P.heads_q + (int64_t)hk * P.group + g, p, i, N, P.n64);
+          RA_BOUNDS(P.status, row >= 0 && row < (int64_t)P.batch * P.heads_q * P.seq && li >= 0 &&
+                                  li + 64 < (int64_t)P.batch * P.heads_q * N * P.n64 * 128, 42);
           const float2 ld = make_float2(P.lse2d[li], P.lse2d[li + 64]);
           pi = exp2f(fmaf(dot_row(q + row * d, ks[warp], d), P.scale_log2, -ld.x));
           ds = pi * (dot_row(dout + row * d, vs[warp], d) - ld.y);

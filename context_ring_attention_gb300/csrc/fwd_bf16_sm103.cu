@@ -257,15 +257,20 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(c.bar(kItemFull + (int)slot));
     if (idx < 0) break;
+    RA_BOUNDS(c.status, idx < P.n_items, 1);
     const WorkItem it = P.items[idx];
     if (!__all_sync(0xffffffffu, wait_bar(c, c.bar(kQEmpty), (u & 1u) ^ 1u, kStatusTimeoutProducer))) break;
     const bool two = it.bh1 >= 0;
+    const int64_t rows_q = (int64_t)P.batch * P.heads_q * P.seq;
     ptx::mbar_arrive_expect_tx_warp(c.bar(kQFull), (two ? 2u : 1u) * kTileBytes);
     const int32_t y0 = (int32_t)((int64_t)it.bh0 * P.seq + (int64_t)it.shard * P.s_n + it.row0);
+    RA_BOUNDS(c.status, it.shard >= 0 && it.shard < P.n_shards && it.row0 >= 0 && it.row0 < P.s_n, 2);
+    RA_BOUNDS(c.status, y0 >= 0 && y0 < rows_q, 3);
     TMA_Q(sbase + kOffQ, tq, c.bar(kQFull), 0, y0);
     TMA_Q(sbase + kOffQ + kHalfBytes, tq, c.bar(kQFull), 64, y0);
     if (two) {
       const int32_t y1 = (int32_t)((int64_t)it.bh1 * P.seq + (int64_t)it.shard * P.s_n + it.row1);
+      RA_BOUNDS(c.status, it.row1 >= 0 && it.row1 < P.s_n && y1 >= 0 && y1 < rows_q, 3);
       TMA_Q(sbase + kOffQ + kTileBytes, tq, c.bar(kQFull), 0, y1);
       TMA_Q(sbase + kOffQ + kTileBytes + kHalfBytes, tq, c.bar(kQFull), 64, y1);
     }
@@ -279,6 +284,9 @@ __device__ void run_producer(const FwdParams& P, const Ctl& c, uint32_t sbase, v
     while (ok && w.t < P.step_hi) {
       const int slot = P.kv_rotated ? it.shard : w.r;  // where the block of step t sits
       const int32_t y = (int32_t)(kv_base + (kGathered ? 0 : (int64_t)slot * P.s_n) + (int64_t)w.kt * kTileRows);
+      RA_BOUNDS(c.status, w.r >= 0 && w.r < P.n_shards && w.kt >= 0 && w.kt < w.nt &&
+                              (int64_t)w.kt * kTileRows < (kGathered ? P.seq : P.s_n), 4);
+      RA_BOUNDS(c.status, y >= 0 && y < (int64_t)P.batch * P.heads_kv * P.seq, 5);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // K tile, then V tile
         const uint32_t s = kv_it % kStages, use = kv_it / kStages;
@@ -341,6 +349,8 @@ __device__ void run_mma(const FwdParams& P, const Ctl& c, uint32_t sbase, volati
   dl.v0 = ptx::desc_lo(sbase + kOffKV, kHalfBytes);
   uint32_t kv_it = 0, pj0 = 0, pj1 = 0;
   const int lane = threadIdx.x & 31;
+  // the column map (S0, S1, O0, O1 = 0, 128, 256, 384) needs all 512 columns from 0
+  RA_BOUNDS(c.status, tmem == 0u && col_o(1) + 128u <= kTmemCols, 6);
   for (uint32_t u = 0;; ++u) {
     const int idx = next_item(c, slots, u, lane);
     if (idx < 0) break;
@@ -461,6 +471,8 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
   const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
   const uint32_t tS = tmem + lane_off + col_s(g);
   const uint32_t tO = tmem + lane_off + col_o(g);
+  RA_BOUNDS(c.status, wq >= 0 && wq < 4 && (tS & 0xFFFFu) + 128u <= kTmemCols && (tO & 0xFFFFu) + 128u <= kTmemCols &&
+                          (tS & 0xFFFFu) + kColP + 64u <= kTmemCols, 7);
   const bool partials = P.o_parts != nullptr;
   const int N = P.n_shards;
   const int64_t rows_all = (int64_t)P.batch * P.heads_q * P.seq;
@@ -478,6 +490,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
     const bool valid = i < P.s_n;
     const int64_t my_pos = pos_of(P.layout, N, P.s_n, p, valid ? i : P.s_n - 1);
     const int64_t out_row = (int64_t)bh * P.seq + (int64_t)p * P.s_n + i;
+    RA_BOUNDS(c.status, !valid || (bh >= 0 && out_row >= 0 && out_row < rows_all), 8);
     int last_t = -1;
     const int t_end = kGathered ? P.step_lo + 1 : P.step_hi;  // gathered: one step
     for (int t = P.step_lo; t < t_end; ++t)
@@ -489,6 +502,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
       const int r = kGathered ? 0 : (p - t + N) % N;
       const int nt = kv_tiles<kGathered>(P, r, it.maxq);
       const int part = t - P.step_lo;  // index of this step's partial
+      RA_BOUNDS(c.status, part >= 0 && part < P.step_hi - P.step_lo, 9);
       if (nt == 0) {
         if (partials && valid) {  // nothing of this block is causal for the tile
           float4* dst = reinterpret_cast<float4*>(P.o_parts + ((int64_t)part * rows_all + out_row) * 128);
@@ -510,6 +524,7 @@ __device__ void run_softmax(const FwdParams& P, const Ctl& c, uint32_t sbase, vo
         open = true;
         int limit = keys - kt * kTileRows;  // keys of this tile the row sees
         limit = limit < 0 ? 0 : (limit > kTileRows ? kTileRows : limit);
+        RA_BOUNDS(c.status, keys >= 0 && keys <= kv_rows && (int64_t)kt * kTileRows < kv_rows, 10);
 
         bool ok = wait_bar(c, c.bar(kSFull + g), sj & 1u, kStatusTimeoutSoftmax);
         ++sj;

@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(kWarps * 32)
     const int slot = P.gathered ? 0 : (P.kv_rotated ? p : r);  // where the block of step t sits
     const float* kb = k + (kv_base + (int64_t)slot * P.s_n) * d;
     const float* vb = v + (kv_base + (int64_t)slot * P.s_n) * d;
+    RA_BOUNDS(P.status, nkeys >= 0 && nkeys <= kv_rows && slot >= 0 && slot < N &&
+                            kv_base + (int64_t)slot * P.s_n + nkeys <= (int64_t)P.batch * P.heads_kv * P.seq, 40);
     for (int64_t j0 = 0; j0 < nkeys; j0 += 32) {
       const int64_t j = j0 + lane;
       float s = -INFINITY;

@@ -210,9 +210,8 @@ extern "C" ra_status ra_fwd_static_status(void* stream) {
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, cudaGetErrorString(e));
   if (word != 0) {
     char msg[200];
-    snprintf(msg, sizeof(msg),
-             "device wait ran out of budget (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 teardown)", word);
-    return fail(RA_ERR_TIMEOUT, msg);
+    const ra_status code = ra::status_word_error(word, msg, sizeof(msg));
+    return fail(code, msg);
   }
   ra::set_last_error("");
   return RA_OK;

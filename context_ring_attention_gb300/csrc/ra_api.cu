@@ -934,7 +934,9 @@ ra_status ra_sync_status(ra_plan_t plan, void* stream) {
   if (e != cudaSuccess) return fail(RA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   if (word != 0) {
     cudaMemset(plan->d_status, 0, sizeof(word));
-    return fail(RA_ERR_TIMEOUT, "device wait ran out of budget (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 teardown)", word);
+    char msg[200];
+    const ra_status code = ra::status_word_error(word, msg, sizeof(msg));
+    return fail(code, "%s", msg);
   }
   return ok();
 }

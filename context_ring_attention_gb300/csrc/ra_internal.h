@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <cstdio>
 #include <cuda_runtime.h>
 
 #include "ra.h"
@@ -193,7 +194,36 @@ enum : uint32_t {
   kStatusTimeoutMma = 1u << 1,
   kStatusTimeoutSoftmax = 1u << 2,
   kStatusTimeoutTeardown = 1u << 3,
+  kStatusTimeouts = 15u,
+  kStatusBounds = 1u << 4,  // debug build: a bounds check failed; bits 8-15 hold the OR of the sites
 };
+
+// Bounds checks of the debug build (-DRA_DEBUG_BOUNDS, libra_debug.so).  A failed check
+// ORs kStatusBounds and its site number (1-255, bits 8-15) into the kernel's status
+// word and the kernel carries on; ra_sync_status then returns RA_ERR_BOUNDS.  The
+// release build compiles the checks out.
+#if defined(RA_DEBUG_BOUNDS)
+#define RA_BOUNDS(status, cond, site)                                                  \
+  do {                                                                                 \
+    if (!(cond)) atomicOr((status), ::ra::kStatusBounds | ((uint32_t)(site) << 8));   \
+  } while (0)
+#else
+#define RA_BOUNDS(status, cond, site) \
+  do {                                \
+  } while (0)
+#endif
+
+// The error a non-zero status word stands for, with its message in msg.
+inline ra_status status_word_error(uint32_t word, char* msg, size_t n) {
+  if (word & kStatusBounds) {
+    snprintf(msg, n, "debug bounds check failed (status word 0x%x; sites OR-ed in bits 8-15: 0x%x)", word,
+             (word >> 8) & 0xFFu);
+    return RA_ERR_BOUNDS;
+  }
+  snprintf(msg, n, "device wait ran out of budget (status bits 0x%x: 1 producer, 2 mma, 4 softmax, 8 teardown)",
+           word);
+  return RA_ERR_TIMEOUT;
+}
 
 // Whether a bf16 problem runs its forward in synchronised rounds: when one key/value
 // head's K and V (S x d x 2 bytes each) exceed 32 MiB, so that CTAs drifting apart

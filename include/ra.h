@@ -68,7 +68,8 @@ typedef enum {
   RA_ERR_UNSUPPORTED = 2,  /* valid problem outside what the kernels handle      */
   RA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed               */
   RA_ERR_TIMEOUT = 4,      /* a device-side wait exceeded its budget (~1 s)      */
-  RA_ERR_NO_DEVICE = 5     /* the plan has no device state (no GPU at plan time) */
+  RA_ERR_NO_DEVICE = 5,    /* the plan has no device state (no GPU at plan time) */
+  RA_ERR_BOUNDS = 6        /* debug build only: a kernel's bounds check failed    */
 } ra_status;
 
 typedef enum {
@@ -358,8 +359,9 @@ ra_status ra_layout_index(int32_t layout, int64_t seq, int32_t n_shards, int64_t
 /*
  * ra_sync_status -- synchronize `stream`, then read and clear the plan's device
  * status word.  Returns RA_ERR_TIMEOUT if a kernel launched with this plan gave
- * up on a device-side wait since the last call, RA_ERR_CUDA on a CUDA error,
- * RA_OK otherwise.
+ * up on a device-side wait since the last call, RA_ERR_BOUNDS if (in the debug
+ * build, libra_debug.so, compiled with RA_DEBUG_BOUNDS) one of its bounds checks
+ * failed, RA_ERR_CUDA on a CUDA error, RA_OK otherwise.
  */
 ra_status ra_sync_status(ra_plan_t plan, void* stream);
 
@@ -399,10 +401,11 @@ ra_status ra_fwd_static(const ra_problem* prob, const void* q, const void* k, co
  * call on the current device.  Like ra_fwd_static, no counterpart on the pages.
  * Synchronizes `stream` (the stream that call ran on), then reads and clears the
  * status word in the static array: RA_ERR_TIMEOUT if that call's kernel gave up
- * on a device-side wait (its O/LSE are then incomplete), RA_OK otherwise or when
- * ra_fwd_static has not run on this device.  It allocates nothing.  The next
- * ra_fwd_static call clears the word, so read it before issuing another.
- * Errors: RA_ERR_TIMEOUT, RA_ERR_NO_DEVICE, RA_ERR_CUDA.
+ * on a device-side wait (its O/LSE are then incomplete), RA_ERR_BOUNDS if a
+ * bounds check of the debug build failed, RA_OK otherwise or when ra_fwd_static
+ * has not run on this device.  It allocates nothing.  The next ra_fwd_static call
+ * clears the word, so read it before issuing another.
+ * Errors: RA_ERR_TIMEOUT, RA_ERR_BOUNDS, RA_ERR_NO_DEVICE, RA_ERR_CUDA.
  */
 ra_status ra_fwd_static_status(void* stream);
 

@@ -39,6 +39,58 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
 
 
+def test_status_names_match_header():
+    with open(os.path.join(ROOT, "include", "ra.h")) as f:
+        text = f.read()
+    codes = {int(v): n for n, v in re.findall(r"\b(RA_(?:OK|ERR_[A-Z_]+))\s*=\s*(\d+)", text)}
+    assert codes == ra._STATUS
+
+
+def test_debug_build_exports_the_same_symbols():
+    from context_ring_attention_gb300 import build
+    if not os.path.exists(build.LIB_DEBUG):
+        build.build(debug=True)
+    dbg = ctypes.CDLL(build.LIB_DEBUG)
+    for n in _declared_symbols():
+        assert hasattr(dbg, n), n
+
+
+def test_status_word_decoding(tmp_path):
+    """The status word -> error mapping that ra_sync_status and ra_fwd_static_status
+    share: the bounds bit wins and reports its sites; otherwise a timeout."""
+    import shutil
+    import subprocess
+    gxx = shutil.which("g++")
+    cuda_inc = "/usr/local/cuda/include"
+    if gxx is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime.h")):
+        pytest.skip("g++ or the CUDA headers are missing")
+    src = tmp_path / "decode.cpp"
+    src.write_text(
+        '#include "ra_internal.h"\n'
+        "int main() {\n"
+        "  char m[200];\n"
+        "  if (ra::status_word_error(ra::kStatusTimeoutMma, m, sizeof m) != RA_ERR_TIMEOUT) return 1;\n"
+        "  if (ra::status_word_error(ra::kStatusBounds | (0x2Au << 8), m, sizeof m) != RA_ERR_BOUNDS) return 2;\n"
+        "  if (std::string(m).find(\"0x2a\") == std::string::npos) return 3;\n"
+        "  if (ra::status_word_error(ra::kStatusBounds | ra::kStatusTimeoutSoftmax, m, sizeof m) != RA_ERR_BOUNDS)"
+        " return 4;\n"
+        "  return 0;\n"
+        "}\n")
+    exe = tmp_path / "decode"
+    csrc = os.path.join(ROOT, "context_ring_attention_gb300", "csrc")
+    res = subprocess.run([gxx, "-std=c++17", "-include", "string", "-I", cuda_inc, "-I", csrc, "-I",
+                          os.path.join(ROOT, "include"), str(src), "-o", str(exe)], capture_output=True, text=True)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert subprocess.run([str(exe)]).returncode == 0
+
+
+def test_library_variant_selects_the_debug_build(monkeypatch):
+    monkeypatch.setenv("RA_LIBRARY_VARIANT", "debug")
+    assert os.path.basename(ra.library_path()) == "libra_debug.so"
+    monkeypatch.delenv("RA_LIBRARY_VARIANT")
+    assert os.path.basename(ra.library_path()) == "libra.so"
+
+
 def test_no_device_plan_refuses_fwd(lib):
     pytest.importorskip("torch")
     import torch
