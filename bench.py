@@ -78,6 +78,22 @@ def clock_peak(sms, sm_mhz):
     return sms * TC_FLOP_PER_CLK_SM * float(sm_mhz) * 1e6 / 1e12
 
 
+# The exponential unit: 32 ex2.approx per clock per SM (measured on a GB300 with 256
+# threads per SM on independent chains: 31.3; the packed bf16x2 and f16x2 forms give
+# the same element rate).  The forward takes one exponential per credited (q, k) pair,
+# i.e. per 4*d = 512 algorithmic FLOPs at d = 128.
+EX2_PER_CLK_SM = 32
+
+
+def exp_rate(flops, head_dim, seconds, sms, sm_mhz):
+    """Exponentials per second of the credited pairs against the unit's rate at the clock."""
+    achieved = flops / (4 * head_dim) / seconds
+    peak = sms * EX2_PER_CLK_SM * float(sm_mhz) * 1e6 if sm_mhz else None
+    return {"achieved_per_s": achieved, "peak_per_s": peak, "frac": achieved / peak if peak else None,
+            "note": (f"one exp per credited (q, k) pair (4 x d FLOPs); peak {sms} SMs x {EX2_PER_CLK_SM} ex2 per SM "
+                     "clock x the median SM clock; masked pairs inside partial tiles also take an exp, uncredited")}
+
+
 # A (batch, key/value head) unit of the end-to-end pipeline needs this many FLOPs
 # (about 0.1 s of forward) before a step is split into such units.
 E2E_UNIT_FLOPS = 2e14
@@ -551,7 +567,8 @@ def run_ours(args, wl):
                      "peak_at_clock_note": (f"{sms} SMs x {TC_FLOP_PER_CLK_SM} dense bf16 FLOP per SM clock x the "
                                             "median SM clock sampled during the timed steps"),
                      "fwd_ms_mean": fwd_mean, "fwd_ms_median": statistics.median(fwd_ms),
-                     "fwd_ms_all": fwd_ms},
+                     "fwd_ms_all": fwd_ms,
+                     "exp_rate": exp_rate(flops, wl.head_dim, fwd_mean * 1e-3, sms, clocks.get("sm_mhz"))},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,

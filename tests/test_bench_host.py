@@ -44,3 +44,12 @@ def test_config_names_the_workload():
     wl = dataclasses.replace(workloads.WORKLOADS["causal_32k_n8"], layouts=("zigzag",))
     cfg = bench.config_of(wl)
     assert cfg["workload"] == "causal_32k_n8" and cfg["layout"] == "zigzag" and cfg["seq"] == 32768
+
+
+def test_exp_rate():
+    # 1M causal zigzag: 9.007e15 FLOP -> 1.759e13 exponentials; over 5.18 s at 1845 MHz
+    r = bench.exp_rate(9007207844675584, 128, 5.18, 152, 1845.0)
+    assert abs(r["achieved_per_s"] - 9007207844675584 / 512 / 5.18) < 1e3
+    assert abs(r["peak_per_s"] - 152 * 32 * 1845e6) < 1.0
+    assert 0.37 < r["frac"] < 0.39
+    assert bench.exp_rate(1e12, 128, 1.0, 152, None)["frac"] is None
