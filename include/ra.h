@@ -381,7 +381,7 @@ ra_status ra_sync_status(ra_plan_t plan, void* stream);
  *     131072), or more than 2^30 (item, ring step) pairs to cost, are rejected
  *     with RA_ERR_UNSUPPORTED.
  *   - Set-up: the first call on a device (with that device current) looks up the
- *     array's device address; make that first call before any stream capture.
+ *     array's device address (a host-side runtime query, made once per device).
  *   - Sharing: every call reuses the array; the status word is cleared at the
  *     start of each call.  Calls whose kernels overlap on the GPU race on the
  *     array and must not be issued; calls from several host threads are
