@@ -23,12 +23,16 @@ FWD_SHAPES = [
     (1, 256, 8, 1, 1, "contiguous", True),
     (1, 320, 2, 1, 8, "zigzag", True),
     (1, 320, 2, 2, 8, "striped", False),
+    (1, 16, 4, 2, 16, "contiguous", True),
+    (1, 32, 4, 2, 16, "zigzag", True),
+    (1, 48, 4, 2, 16, "striped", False),
 ]
 BWD_SHAPES = [
     (1, 900, 4, 2, 3, "striped", True),
     (1, 320, 2, 1, 8, "zigzag", True),
     (2, 640, 2, 2, 4, "contiguous", False),
     (1, 768, 6, 2, 2, "zigzag", True),
+    (1, 48, 4, 2, 16, "striped", True),
 ]
 
 
