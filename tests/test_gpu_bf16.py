@@ -168,3 +168,38 @@ def test_bf16_shards_of_a_few_rows(s_n, layout, causal):
     if layout == "zigzag" and s_n % 2:
         pytest.skip("zigzag needs 2N | S")
     _run(1, n * s_n, 4, 2, n, layout, causal, seed=70 + s_n)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bf16_several_dominant_keys_at_rounding_midpoints(causal):
+    # Rows 64..127 see four dominant keys (positions 3, 10, 40, 60) whose weights
+    # relative to the largest are about 1, 1 - 2^-9, 1 - 3*2^-9 and 1 - 5*2^-9: the
+    # last three sit at or beside midpoints of bf16 rounding, where P's rounding error
+    # is largest, and the row-sum correction covers only the largest key.  Their values
+    # are +4, -4, +4, -4 in every column, so that O is near zero and its own bf16
+    # rounding negligible; every other key is 28 natural-log units below them.  The
+    # bf16 rounding of the three weights moves O by at most 3 * 2^-9 * 4 / 4 (about
+    # 6e-3), inside the 2e-2 tolerance.
+    B, S, H, d = 1, 128, 1, 128
+    q, k, v = workloads.small_inputs(B, S, H, H, d, seed=37, device="cuda", dtype="bf16")
+    scale = 1.0 / np.sqrt(d)
+    q[0, 0, 64:] = 0
+    q[0, 0, 64:, 0] = 8.0    # base score 8 * 40 * scale = 28.3 for the dominant keys
+    q[0, 0, 64:, 1] = 64.0   # carries the small offsets ln(ratio) through k[:, 1]
+    k[0, 0] = 0
+    dominant = ((3, 1.0, 4.0), (10, 1 - 2.0 ** -9, -4.0), (40, 1 - 3 * 2.0 ** -9, 4.0), (60, 1 - 5 * 2.0 ** -9, -4.0))
+    for pos, ratio, value in dominant:
+        k[0, 0, pos, 0] = 40.0
+        k[0, 0, pos, 1] = np.log(ratio) / (64.0 * scale)
+        v[0, 0, pos] = value
+    plan = ra.ra_plan(B, S, H, H, d, 1, "contiguous", causal, "bf16")
+    o, lse = ra.ra_fwd(plan, q, k, v)
+    ra.ra_sync_status(plan)
+    ow, lw = oracle.full_attention(to64(q), to64(k), to64(v), causal=causal)
+    err = np.abs(to64(o)[0, 0, 64:] - ow[0, 0, 64:]).max()
+    print(f"several dominant keys, causal={causal}: max-abs error {err:.3e} on rows 64..127")
+    assert err <= 3 * 2.0 ** -9 + 5e-4
+    # O is built to be near zero on those rows, so the relative-RMS part of the parity
+    # bound says nothing here; the absolute parts apply to the whole tensor.
+    assert np.abs(to64(o) - ow).max() <= 2e-2
+    assert np.abs(to64(lse) - lw).max() <= 2e-2
