@@ -220,3 +220,10 @@ def test_bf16_backward_shards_of_a_few_rows(s_n, layout):
     got, want = _run(1, 16 * s_n, 4, 2, 16, layout, True, seed=80 + s_n)
     for name, g_, w_ in zip(("dQ", "dK", "dV"), got, want):
         _close(to64(g_), w_, f"{name} s_n={s_n} {layout}")
+
+
+@pytest.mark.parametrize("d", [13, 128])
+def test_f32_backward_head_dim_edges(d):
+    got, want = _run(1, 96, 4, 2, 4, "striped", True, seed=90 + d, dtype="f32", d=d)
+    for name, g_, w_ in zip(("dQ", "dK", "dV"), got, want):
+        _close(to64(g_), w_, f"f32 d={d} {name}", rel_rms=1e-5, max_rel=F32_MAX_REL)

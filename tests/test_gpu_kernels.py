@@ -120,3 +120,12 @@ def test_f32_layouts_gqa_partials(layout, causal):
     torch.cuda.synchronize()
     assert_f32_close(to64(om), to64(o), "merge vs fused O")
     assert_f32_close(to64(lm), to64(lse), "merge vs fused LSE")
+
+
+@pytest.mark.parametrize("d", [13, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_f32_head_dim_edges(d, causal):
+    # the SIMT fp32 path at its largest head dimension and at one that is not a
+    # multiple of 4 (the lanes' column loops end mid-warp), striped with GQA
+    q, k, v = workloads.small_inputs(1, 96, 4, 2, d, seed=13 + d, device="cuda", dtype="f32")
+    _f32_case(q, k, v, 4, "striped", causal)
