@@ -15,6 +15,10 @@ contiguity and device before anything is launched.
 
 Tensors are ``[B, H, S, d]`` contiguous with S in layout order (shard p owns rows
 [p*S/N, (p+1)*S/N)); ``ra_layout_perm`` moves natural order <-> layout order.
+
+With RA_LIBRARY_VARIANT=debug in the environment the binding loads libra_debug.so
+instead: the same library with the kernels' bounds checks compiled in, which
+``ra_sync_status`` reports as RaError(RA_ERR_BOUNDS).
 """
 
 import ctypes
