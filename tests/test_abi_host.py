@@ -118,6 +118,9 @@ def test_no_device_plan_refuses_fwd(lib):
     # planner limits: N^2 x query tiles above 2^30; bf16 work lists above 2^27 entries
     (dict(seq=32767 * 1024, n_shards=32767, heads_q=1, heads_kv=1), 2),
     (dict(seq=4096 * 1024, n_shards=4096, heads_q=2, heads_kv=1), 2),
+    # B * Hq * S rows must fit the kernels' 32-bit row coordinates: 32 x 2^26 = 2^31
+    (dict(seq=1 << 26, heads_q=32, heads_kv=8), 2),
+    (dict(seq=1 << 26, heads_q=32, heads_kv=8, dtype="f32", head_dim=64), 2),
 ])
 def test_plan_rejects(lib, kw, status):
     args = dict(batch=1, seq=1024, heads_q=4, heads_kv=2, head_dim=128, n_shards=8, layout="contiguous",
